@@ -1,0 +1,414 @@
+"""Benchmark of the CSA indexer hot path (fused score + per-row top-k).
+
+Default workload: long-context prefill, B=2, S=16384, compress_rate 4
+(W=4096), H=64, D=128, top_k=2048, seeded N(0,1) bf16 inputs; one step is one
+``csa_index_fused`` call over the whole batch (scores never written to HBM).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  ``value`` is useful causal TFLOP/s,
+2*H*D*(visible (s,t) pairs) / time, with inputs resident in HBM; ``e2e`` is
+the same metric with the host<->device copies of each step's inputs and
+result inside the timed region.  Under torchrun every rank runs its own
+replica of the workload (rows and batches are independent; no collective on
+the data path), so scaling is weak and ``value`` sums all ranks' work over
+the slowest rank's time.  ``--impl reference`` times the CPU oracle instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from csa_inputs import WORKLOADS, Inputs, make_inputs  # noqa: E402
+
+METRIC = "indexer useful TFLOP/s and query rows/s at S=16K; % of bf16 tensor peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ----------------------------------------------------------------------------- work accounting
+def visible_counts(inp: Inputs) -> np.ndarray:
+    """v[b,s]: visible entries per row (future mask and segment ids), counted
+    from the inputs with plain integer arithmetic."""
+    wl = inp.wl
+    start = np.zeros(wl.B, dtype=np.int64) if inp.q_start is None else inp.q_start.numpy()
+    pos = start[:, None] + np.arange(wl.S)[None, :]
+    thr = np.clip((pos + 1) // wl.compress_rate, 0, wl.W)
+    if inp.q_seg is None:
+        return thr
+    v = np.zeros((wl.B, wl.S), dtype=np.int64)
+    kv = inp.kv_seg.numpy()
+    qs = inp.q_seg.numpy()
+    for b in range(wl.B):
+        for seg in np.unique(qs[b]):
+            match = np.cumsum(kv[b] == seg)  # entries of this segment among t < n
+            rows = qs[b] == seg
+            tb = thr[b, rows]
+            v[b, rows] = np.where(tb > 0, match[np.maximum(tb - 1, 0)], 0)
+    return v
+
+
+def work(inp: Inputs):
+    wl = inp.wl
+    v = visible_counts(inp)
+    pairs = int(v.sum())
+    nontrivial = int(v[v > wl.top_k].sum())
+    per_pair = 2.0 * wl.H * wl.D
+    return dict(pairs=pairs, flops=per_pair * pairs, flops_nontrivial=per_pair * nontrivial,
+                rows=wl.B * wl.S, nontrivial_rows=int((v > wl.top_k).sum()))
+
+
+def read_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            with open(path) as f:
+                return json.load(f), "measured"
+        except Exception:
+            pass
+    return FALLBACK_PEAKS, "fallback"
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples every 200 ms while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200",
+                 "-i", str(self.dev)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- distributed plumbing
+def dist_setup(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+        return rank, world, local, dist
+    return 0, 1, 0, None
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def max_over_ranks(x: float, dist) -> float:
+    if dist is None:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x: float, dist) -> float:
+    if dist is None:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- CPU oracle timing
+def oracle_sample(inp: Inputs, budget_s: float, block: int = 256, seed: int = 0):
+    """Time the CPU oracle (fp64 scores + full-sort selection) on random row
+    blocks of batch 0 until `budget_s` seconds pass; returns rate figures."""
+    from oracle import csa_oracle as O
+
+    wl = inp.wl
+    q = inp.q[0:1].double().numpy()
+    k = inp.k[0:1].double().numpy()
+    w = inp.w[0:1].double().numpy()
+    q_start = None if inp.q_start is None else inp.q_start[0:1].numpy()
+    q_seg = None if inp.q_seg is None else inp.q_seg[0:1].numpy()
+    kv_seg = None if inp.kv_seg is None else inp.kv_seg[0:1].numpy()
+    v = visible_counts(inp)[0]
+    rng = np.random.default_rng(seed)
+    t0 = time.perf_counter()
+    rows_done, pairs_done = 0, 0
+    while True:
+        rows = np.sort(rng.choice(wl.S, size=min(block, wl.S), replace=False))
+        sc = O.index_scores(q, k, w, wl.scale, wl.compress_rate, q_start, q_seg, kv_seg, rows=rows)
+        O.select_topk(sc, wl.top_k)
+        rows_done += len(rows)
+        pairs_done += int(v[rows].sum())
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    flops = 2.0 * wl.H * wl.D * pairs_done
+    return dict(seconds=el, rows=rows_done, pairs=pairs_done, tflops=flops / el / 1e12, rows_per_s=rows_done / el)
+
+
+def run_reference(args, wl, inp):
+    budget = max(0.5, min(10.0, 150.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        oracle_sample(inp, budget * 0.25, block=64)
+    res = [oracle_sample(inp, budget, block=64, seed=i) for i in range(args.steps)]
+    secs = sum(r["seconds"] for r in res)
+    flops = sum(2.0 * wl.H * wl.D * r["pairs"] for r in res)
+    rows = sum(r["rows"] for r in res)
+    value = flops / secs / 1e12
+    cores = os.cpu_count()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_dict(wl, args.gpus),
+        "rows_per_s": rows / secs,
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{rows} random query rows of batch 0 ({args.steps} steps of about "
+                                   f"{budget:.1f} s), fp64 scores + full-sort selection"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_dict(wl, n_gpus):
+    return {"workload": wl.name, "B": wl.B, "S": wl.S, "W": wl.W, "H": wl.H, "D": wl.D,
+            "compress_rate": wl.compress_rate, "top_k": wl.top_k, "w_dtype": wl.w_dtype,
+            "q_start": wl.q_start, "docs": list(wl.docs) if wl.docs else None,
+            "global_batch": wl.B * n_gpus, "seq_len": wl.S,
+            "parallelism": f"replicas x{n_gpus}" if n_gpus > 1 else "single GPU",
+            "l2": "no flush: inputs larger than L2 (q is {:.0f} MiB)".format(
+                wl.B * wl.H * wl.S * wl.D * 2 / 2**20)}
+
+
+# ----------------------------------------------------------------------------- GPU arm
+def run_ours(args, wl, inp):
+    import sparse_attention_indexer_csa_gb300 as csa
+
+    rank, world, local, dist = dist_setup(args.gpus)
+    if not torch.cuda.is_available():
+        raise RuntimeError("bench.py needs a CUDA GPU for the library arm")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    csa.load()
+    stream = torch.cuda.current_stream(dev)
+    wk = work(inp)
+
+    q, k, w = inp.q.to(dev), inp.k.to(dev), inp.w.to(dev)
+    q_seg = None if inp.q_seg is None else inp.q_seg.to(dev)
+    kv_seg = None if inp.kv_seg is None else inp.kv_seg.to(dev)
+    q_start = None if inp.q_start is None else inp.q_start.to(dev)
+    p = csa.make_problem(q, k, w, wl.scale, wl.compress_rate, wl.top_k)
+    idx = torch.empty(wl.B, wl.S, wl.top_k, dtype=torch.int32, device=dev)
+    ws_bytes = csa.workspace_size(p, 1)
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev) if ws_bytes else None
+    launches_per_step = 2 if ws_bytes else 1
+
+    def step():
+        st = csa.index_fused_raw(p, q, k, w, q_seg, kv_seg, q_start, idx, None, ws, stream)
+        if st != csa.CSA_OK:
+            raise RuntimeError(f"csa_index_fused returned {st}")
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if csa.device_status(stream) != csa.CSA_OK:
+        raise RuntimeError("device status word reports an error after warm-up")
+
+    # ---- device-resident timing (K steps, per-step events on the launch stream)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    clocks = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ
+                          else local)
+    barrier(dist)
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.25)  # let the sampler take its first reading
+    t_all0 = torch.cuda.Event(enable_timing=True)
+    t_all1 = torch.cuda.Event(enable_timing=True)
+    t_all0.record(stream)
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    t_all1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    barrier(dist)
+    total_ms = t_all0.elapsed_time(t_all1)
+    launch_ms = [a.elapsed_time(b) for a, b in ev]
+    total_ms = max_over_ranks(total_ms, dist)
+    ms_step = total_ms / args.steps
+    if csa.device_status(stream) != csa.CSA_OK:
+        raise RuntimeError("device status word reports an error after the timed region")
+
+    # ---- end to end: pinned host inputs -> device, call, result -> pinned host
+    hq, hk, hw = inp.q.pin_memory(), inp.k.pin_memory(), inp.w.pin_memory()
+    hqs = None if inp.q_seg is None else inp.q_seg.pin_memory()
+    hks = None if inp.kv_seg is None else inp.kv_seg.pin_memory()
+    hst = None if inp.q_start is None else inp.q_start.pin_memory()
+    hidx = torch.empty(idx.shape, dtype=idx.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hw, hqs, hks, hst) if t is not None)
+    d2h = hidx.numel() * hidx.element_size()
+
+    def e2e_step():
+        q.copy_(hq, non_blocking=True)
+        k.copy_(hk, non_blocking=True)
+        w.copy_(hw, non_blocking=True)
+        if hqs is not None:
+            q_seg.copy_(hqs, non_blocking=True)
+            kv_seg.copy_(hks, non_blocking=True)
+        if hst is not None:
+            q_start.copy_(hst, non_blocking=True)
+        step()
+        hidx.copy_(idx, non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, 10))
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(dist)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, dist)
+
+    total_flops = sum_over_ranks(wk["flops"], dist)
+    total_rows = sum_over_ranks(wk["rows"], dist)
+    value = total_flops / (ms_step * 1e-3) / 1e12
+    peaks, peak_src = read_peaks()
+    avg_launch_ms = sum(launch_ms) / len(launch_ms)
+    if ws_bytes:
+        # two kernels per step: the score kernel dominates; report the step
+        achieved = wk["flops_nontrivial"] / (avg_launch_ms * 1e-3) / 1e12
+    else:
+        achieved = wk["flops_nontrivial"] / (avg_launch_ms * 1e-3) / 1e12
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    bound, unit = "tensor", "TFLOP/s"
+    traffic = None
+    if wl.name.startswith("decode"):
+        # k streaming bound: algorithmic bytes = k + q + w + scores write/read + idx
+        bytes_alg = (wl.B * wl.W * wl.D * 2 + wl.B * wl.H * wl.S * wl.D * 2 + wl.B * wl.S * wl.H * 2
+                     + 2 * wl.B * wl.S * wl.W * 4 + wl.B * wl.S * wl.top_k * 4)
+        achieved = bytes_alg / (avg_launch_ms * 1e-3) / 1e9
+        peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+        bound, unit = "hbm", "GB/s"
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": config_dict(wl, world),
+        "rows_per_s": total_rows / (ms_step * 1e-3),
+        "useful_pairs": wk["pairs"], "nontrivial_rows": wk["nontrivial_rows"],
+        "tflops_nontrivial_rows": wk["flops_nontrivial"] / (ms_step * 1e-3) / 1e12,
+        "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+                     "frac": achieved / peak, "traffic": traffic,
+                     "peak_source": f"{peak_src} ({'MEASURED_PEAKS.json' if peak_src == 'measured' else 'recipe fallback'})",
+                     "achieved_counts": "2*H*D per visible pair of rows with visible > top_k (rows at or below "
+                                        "top_k are emitted without scores)" if bound == "tensor" else
+                                        "k + q + w bytes read, scores written and re-read, indices written"},
+        "e2e": {"value": total_flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cb = oracle_sample(inp, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": cb["tflops"], "unit": "TFLOP/s", "cores": os.cpu_count(),
+                                "kind": "oracle",
+                                "sample": f"{cb['rows']} random query rows of batch 0 in {cb['seconds']:.1f} s, "
+                                          f"fp64 scores + full-sort selection ({cb['rows_per_s']:.1f} rows/s)"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="prefill_16k", choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    wl = WORKLOADS[args.workload]
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        inp = make_inputs(wl.with_(seed=wl.seed + rank))
+        run_reference(args, wl, inp)
+        return
+    inp = make_inputs(wl.with_(seed=wl.seed + rank))
+    run_ours(args, wl, inp)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,130 @@
+/*
+ * csa_index.h -- C ABI of the GB300 (sm_103a) CSA indexer library.
+ *
+ * The library computes the DeepSeek-V4 CSA / StreamIndex indexer hot path:
+ *
+ *   score[b,s,t] = sum_h w[b,s,h] * ReLU(scale * <q[b,h,s,:], k[b,t,:]>)
+ *
+ * (the head-reduced indexer score of "Add StreamIndex Kernel for CSA
+ * [Deepseek v4]", Description and BlockSpec review hunk: q [B,H,S,D],
+ * compressed [B,W,D], weights [B,S,H] -> scores [B,S,W]; the activation is
+ * not named there and is taken to be ReLU), masked by the future mask
+ * t >= (pos+1) // compress_rate and by the packed-document segment mask of
+ * "DSV4: Add indexer_save_selection and indexer_sharded_topk" (mask review
+ * hunk), followed by a per-row top-k selection of entry indices (same page,
+ * Description: the selection handed to sparse attention).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - All tensor pointers are DEVICE pointers owned by the caller, contiguous
+ *    row-major, with 16-byte aligned bases.  The library never allocates,
+ *    frees or synchronises in these calls; work is enqueued on `stream`
+ *    (a cudaStream_t passed as void*; NULL = the legacy default stream) on
+ *    the current device.
+ *  - Arguments are checked on the host before anything is launched; a bad
+ *    argument returns CSA_ERR_INVALID_ARG, a valid but unimplemented shape
+ *    returns CSA_ERR_UNSUPPORTED.  There is no fallback path.
+ *  - A launch failure returns CSA_ERR_CUDA.  Every wait inside a kernel is
+ *    bounded; a wait that gives up records CSA_ERR_TIMEOUT in a device status
+ *    word, read (and cleared) by csa_index_device_status().
+ *  - Position of query row s of batch b: pos = q_start[b] + s (q_start NULL
+ *    means 0).  Entry t is visible from row s iff
+ *        t < min(W, (pos + 1) / compress_rate)                (future mask)
+ *    and, when segment ids are given, q_seg[b,s] == kv_seg[b,t].
+ *  - Selection: among visible entries, the min(top_k, visible) largest
+ *    scores; equal scores go to the lower entry index and compare by value
+ *    (-0.0 == +0.0).  Each row's indices are written in ascending order and
+ *    padded with -1 up to top_k.
+ */
+#ifndef CSA_INDEX_H
+#define CSA_INDEX_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  CSA_OK = 0,
+  CSA_ERR_INVALID_ARG = 1, /* null pointer, bad size, misaligned base, scale <= 0 ... */
+  CSA_ERR_UNSUPPORTED = 2, /* valid problem outside the implemented (H, D, W) set   */
+  CSA_ERR_CUDA = 3,        /* a CUDA runtime/driver call or a launch failed          */
+  CSA_ERR_TIMEOUT = 4,     /* a bounded in-kernel wait gave up (device status word)  */
+  CSA_ERR_DEVICE = 5       /* the kernel recorded another device-side error          */
+} csa_status;
+
+typedef enum { CSA_BF16 = 0, CSA_F32 = 1 } csa_dtype;
+
+/* Problem description (all sizes in elements).
+ *   B  batch, H indexer heads, S query rows per batch, D head dim,
+ *   W  compressed entries per batch (the compressed KV length),
+ *   compress_rate  tokens per compressed entry (>= 1),
+ *   scale  > 0, applied to q.k inside the ReLU (e.g. D^-0.5),
+ *   top_k  >= 1 (may exceed the visible count or W: -1 padding),
+ *   w_dtype  storage type of the weights (csa_dtype).               */
+typedef struct {
+  int32_t B, H, S, D, W;
+  int32_t compress_rate;
+  float scale;
+  int32_t top_k;
+  int32_t w_dtype;
+} csa_problem;
+
+/* Scores.  q [B,H,S,D] bf16, k [B,W,D] bf16, w [B,S,H] (w_dtype),
+ * q_seg [B,S] int32 or NULL, kv_seg [B,W] int32 or NULL (both or neither),
+ * q_start [B] int64 or NULL.  Writes scores [B,S,W] fp32, -inf where masked.
+ * Defined by the score formula above ("Add StreamIndex Kernel for CSA
+ * [Deepseek v4]", Description; masks per "DSV4: Add indexer_save_selection
+ * and indexer_sharded_topk", mask review hunk).
+ * Supported: (H, D) in {(64, 128), (4, 32)}, any B, S, W >= 1.           */
+csa_status csa_index_score(const csa_problem* p, const void* q, const void* k, const void* w,
+                           const int32_t* q_seg, const int32_t* kv_seg, const int64_t* q_start,
+                           float* scores, void* stream);
+
+/* Selection only, from precomputed scores [B,S,W] fp32 (an entry is visible
+ * iff its score > -inf).  Writes idx [B,S,top_k] int32 (selection rule
+ * above; "DSV4: Add indexer_save_selection and indexer_sharded_topk",
+ * Description).  workspace may be NULL when csa_index_workspace_size(p, 0)
+ * returns 0 (it does for every supported W).  Supported: W <= 49152.     */
+csa_status csa_index_topk(const csa_problem* p, const float* scores, int32_t* idx,
+                          void* workspace, size_t workspace_bytes, void* stream);
+
+/* Scores and selection in one call: same inputs as csa_index_score, writes
+ * idx [B,S,top_k] int32.  For W <= 4096 the scores stay in on-chip memory
+ * (never written to HBM) unless scores_dbg [B,S,W] fp32 is non-NULL, in
+ * which case the exact fp32 scores the selection used are also written
+ * there.  For larger W (decode-style problems) the scores go through
+ * `workspace` (csa_index_workspace_size(p, 1) bytes, device memory owned by
+ * the caller) and a second selection pass.                                */
+csa_status csa_index_fused(const csa_problem* p, const void* q, const void* k, const void* w,
+                           const int32_t* q_seg, const int32_t* kv_seg, const int64_t* q_start,
+                           int32_t* idx, float* scores_dbg, void* workspace,
+                           size_t workspace_bytes, void* stream);
+
+/* Bytes of device workspace an entry point needs: which = 0 for
+ * csa_index_topk, 1 for csa_index_fused.  Returns 0 when none is needed or
+ * the problem is invalid.                                                 */
+size_t csa_index_workspace_size(const csa_problem* p, int32_t which);
+
+/* Synchronises `stream`, then reads and clears the device status word of
+ * the current device: CSA_OK, CSA_ERR_TIMEOUT (a bounded wait gave up) or
+ * CSA_ERR_DEVICE.  CSA_ERR_CUDA if the synchronisation itself failed.     */
+csa_status csa_index_device_status(void* stream);
+
+/* Runs a kernel whose single wait can never be satisfied, bounded by
+ * `timeout_us` microseconds; it must give up, record CSA_ERR_TIMEOUT and
+ * return.  Used to test the give-up path without faulting a GPU.          */
+csa_status csa_index_selftest_timeout(uint32_t timeout_us, void* stream);
+
+/* Static string for a status code. */
+const char* csa_status_string(csa_status s);
+
+/* ABI version (major * 100 + minor). */
+int32_t csa_index_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* CSA_INDEX_H */

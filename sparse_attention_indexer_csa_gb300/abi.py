@@ -1,0 +1,192 @@
+"""ctypes binding of ``libcsa_index.so`` (the C ABI of ``include/csa_index.h``).
+
+Argument marshalling only: tensors are passed as raw pointers with the
+caller's CUDA stream, every step of the indexer runs in the library's
+kernels.  There is no fallback: if the library is missing or a call fails,
+an exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libcsa_index.so")
+
+CSA_OK, CSA_ERR_INVALID_ARG, CSA_ERR_UNSUPPORTED, CSA_ERR_CUDA, CSA_ERR_TIMEOUT, CSA_ERR_DEVICE = range(6)
+CSA_BF16, CSA_F32 = 0, 1
+
+EXPORTED = (
+    "csa_index_score",
+    "csa_index_topk",
+    "csa_index_fused",
+    "csa_index_workspace_size",
+    "csa_index_device_status",
+    "csa_index_selftest_timeout",
+    "csa_status_string",
+    "csa_index_abi_version",
+)
+
+
+class CsaError(RuntimeError):
+    def __init__(self, fn: str, status: int, msg: str):
+        super().__init__(f"{fn} failed: status {status} ({msg})")
+        self.status = status
+
+
+class Problem(ctypes.Structure):
+    """Mirror of ``csa_problem``."""
+
+    _fields_ = [
+        ("B", ctypes.c_int32), ("H", ctypes.c_int32), ("S", ctypes.c_int32),
+        ("D", ctypes.c_int32), ("W", ctypes.c_int32), ("compress_rate", ctypes.c_int32),
+        ("scale", ctypes.c_float), ("top_k", ctypes.c_int32), ("w_dtype", ctypes.c_int32),
+    ]
+
+
+_lib = None
+
+
+def load(path: Optional[str] = None) -> ctypes.CDLL:
+    """Load the library (once).  Raises if it has not been built."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(f"{p} is missing: build it with sparse_attention_indexer_csa_gb300.build.build()")
+    lib = ctypes.CDLL(p)
+    vp, i32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
+    P = ctypes.POINTER(Problem)
+    lib.csa_index_score.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp]
+    lib.csa_index_topk.argtypes = [P, vp, vp, vp, sz, vp]
+    lib.csa_index_fused.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.csa_index_workspace_size.argtypes = [P, i32]
+    lib.csa_index_workspace_size.restype = sz
+    lib.csa_index_device_status.argtypes = [vp]
+    lib.csa_index_selftest_timeout.argtypes = [ctypes.c_uint32, vp]
+    lib.csa_status_string.argtypes = [i32]
+    lib.csa_status_string.restype = ctypes.c_char_p
+    lib.csa_index_abi_version.restype = i32
+    for name in ("csa_index_score", "csa_index_topk", "csa_index_fused", "csa_index_device_status",
+                 "csa_index_selftest_timeout"):
+        getattr(lib, name).restype = i32
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load().csa_status_string(status).decode()
+
+
+def _check(fn: str, status: int):
+    if status != CSA_OK:
+        raise CsaError(fn, status, status_string(status))
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("tensors passed to the library must live on the GPU")
+    if not t.is_contiguous():
+        raise ValueError("tensors passed to the library must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    return ctypes.c_void_p(handle)
+
+
+def make_problem(q: torch.Tensor, k: torch.Tensor, w: torch.Tensor, scale: float, compress_rate: int,
+                 top_k: int = 1) -> Problem:
+    B, H, S, D = q.shape
+    W = k.shape[1]
+    wd = {torch.bfloat16: CSA_BF16, torch.float32: CSA_F32}.get(w.dtype)
+    if wd is None:
+        raise ValueError("weights must be bf16 or fp32")
+    return Problem(B, H, S, D, W, int(compress_rate), float(scale), int(top_k), wd)
+
+
+# ----------------------------------------------------------------------------- raw C-ABI calls
+def index_score_raw(p: Problem, q, k, w, q_seg, kv_seg, q_start, scores, stream=None) -> int:
+    return load().csa_index_score(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(w), _ptr(q_seg), _ptr(kv_seg),
+                                  _ptr(q_start), _ptr(scores), _stream(stream))
+
+
+def index_topk_raw(p: Problem, scores, idx, workspace=None, stream=None) -> int:
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    return load().csa_index_topk(ctypes.byref(p), _ptr(scores), _ptr(idx), _ptr(workspace), nbytes,
+                                 _stream(stream))
+
+
+def index_fused_raw(p: Problem, q, k, w, q_seg, kv_seg, q_start, idx, scores_dbg=None, workspace=None,
+                    stream=None) -> int:
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    return load().csa_index_fused(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(w), _ptr(q_seg), _ptr(kv_seg),
+                                  _ptr(q_start), _ptr(idx), _ptr(scores_dbg), _ptr(workspace), nbytes,
+                                  _stream(stream))
+
+
+def workspace_size(p: Problem, which: int) -> int:
+    return int(load().csa_index_workspace_size(ctypes.byref(p), which))
+
+
+def device_status(stream=None) -> int:
+    return int(load().csa_index_device_status(_stream(stream)))
+
+
+def selftest_timeout(timeout_us: int, stream=None) -> int:
+    return int(load().csa_index_selftest_timeout(timeout_us, _stream(stream)))
+
+
+# ----------------------------------------------------------------------------- tensor-level helpers
+def index_score(q, k, w, scale, compress_rate, q_seg=None, kv_seg=None, q_start=None, out=None, stream=None):
+    """Scores [B,S,W] fp32 (-inf where masked) on the GPU."""
+    p = make_problem(q, k, w, scale, compress_rate)
+    if out is None:
+        out = torch.empty(p.B, p.S, p.W, dtype=torch.float32, device=q.device)
+    _check("csa_index_score", index_score_raw(p, q, k, w, q_seg, kv_seg, q_start, out, stream))
+    return out
+
+
+def index_topk(scores, top_k, out=None, stream=None):
+    """Per-row selection from scores [B,S,W] fp32 -> idx [B,S,top_k] int32."""
+    B, S, W = scores.shape
+    p = Problem(B, 1, S, 1, W, 1, 1.0, int(top_k), CSA_F32)
+    if out is None:
+        out = torch.empty(B, S, top_k, dtype=torch.int32, device=scores.device)
+    _check("csa_index_topk", index_topk_raw(p, scores, out, None, stream))
+    return out
+
+
+def index_fused(q, k, w, scale, compress_rate, top_k, q_seg=None, kv_seg=None, q_start=None, out=None,
+                scores_dbg=None, workspace=None, stream=None):
+    """Scores and selection in one call -> idx [B,S,top_k] int32."""
+    p = make_problem(q, k, w, scale, compress_rate, top_k)
+    if out is None:
+        out = torch.empty(p.B, p.S, p.top_k, dtype=torch.int32, device=q.device)
+    need = workspace_size(p, 1)
+    if need and workspace is None and scores_dbg is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    _check("csa_index_fused", index_fused_raw(p, q, k, w, q_seg, kv_seg, q_start, out, scores_dbg,
+                                              workspace, stream))
+    return out
+
+
+def index_decode(q, k, w, scale, compress_rate, top_k, q_start, q_seg=None, kv_seg=None, **kw):
+    """Autoregressive selection: one query row per sequence.
+
+    The segment mask is not applied in autoregressive mode ("DSV4: Add
+    indexer_save_selection and indexer_sharded_topk", review of the decode
+    mask), so segment ids given here are ignored.
+    """
+    del q_seg, kv_seg
+    return index_fused(q, k, w, scale, compress_rate, top_k, None, None, q_start, **kw)

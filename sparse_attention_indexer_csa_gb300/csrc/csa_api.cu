@@ -1,0 +1,257 @@
+// csa_api.cu -- the C ABI declared in include/csa_index.h: argument checks,
+// TMA tensor maps, choice of kernel instantiation and launches.  Nothing here
+// computes any part of the indexer; every step runs in the kernels.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/csa_index.h"
+#include "csa_internal.h"
+
+namespace csa {
+namespace {
+
+constexpr int kFusedMaxW = 4096;   // shared-memory score rows of the fused kernel
+constexpr int kTopkMaxW = 49152;   // one row staged in shared memory by the top-k kernel
+constexpr int kDecodeChunkTiles = 8;
+constexpr unsigned long long kWaitNs = 2000000000ull;  // 2 s per wait before giving up
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+csa_status check_problem(const csa_problem* p) {
+  if (p == nullptr) return CSA_ERR_INVALID_ARG;
+  if (p->B < 1 || p->H < 1 || p->S < 1 || p->D < 1 || p->W < 1) return CSA_ERR_INVALID_ARG;
+  if (p->compress_rate < 1 || p->top_k < 1) return CSA_ERR_INVALID_ARG;
+  if (!(p->scale > 0.f) || !std::isfinite(p->scale)) return CSA_ERR_INVALID_ARG;
+  if (p->w_dtype != CSA_BF16 && p->w_dtype != CSA_F32) return CSA_ERR_INVALID_ARG;
+  const double rows = (double)p->B * (double)p->S;
+  if (rows * (double)p->W > 4.0e18 || rows * (double)p->top_k > 4.0e18) return CSA_ERR_INVALID_ARG;
+  return CSA_OK;
+}
+
+csa_status check_inputs(const csa_problem* p, const void* q, const void* k, const void* w, const int32_t* q_seg,
+                        const int32_t* kv_seg, const int64_t* q_start) {
+  if (q == nullptr || k == nullptr || w == nullptr) return CSA_ERR_INVALID_ARG;
+  if ((q_seg == nullptr) != (kv_seg == nullptr)) return CSA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16)) return CSA_ERR_INVALID_ARG;  // TMA bases
+  if (!aligned(w, p->w_dtype == CSA_F32 ? 4 : 2)) return CSA_ERR_INVALID_ARG;
+  if (q_seg && (!aligned(q_seg, 4) || !aligned(kv_seg, 4))) return CSA_ERR_INVALID_ARG;
+  if (q_start && !aligned(q_start, 8)) return CSA_ERR_INVALID_ARG;
+  return CSA_OK;
+}
+
+bool shape_supported(const csa_problem* p) {
+  return (p->H == 64 && p->D == 128) || (p->H == 4 && p->D == 32);
+}
+
+// Single-row problems use the R = 1 kernel with tile chunks, which keeps every
+// SM busy streaming k; everything else uses blocks of four query rows.
+bool use_row_kernel(const csa_problem* p) { return p->S <= 2 && p->H == 64 && p->D == 128; }
+
+bool fused_in_smem(const csa_problem* p) { return !use_row_kernel(p) && p->W <= kFusedMaxW; }
+
+int num_sms() {
+  static int cached[64];
+  static std::once_flag flags[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  std::call_once(flags[dev], [dev] {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) n = 0;
+    cached[dev] = n;
+  });
+  return cached[dev];
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag flag;
+  std::call_once(flag, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// q [B,H,S,D] bf16 viewed as dims (D, H, S, B) so one box {KC, H, R, 1}
+// lands as R*H rows ordered (row j, head h) -> j*H + h.
+bool make_q_map(CUtensorMap* m, const csa_problem* p, const void* q, int R) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const int KC = (p->D % 64 == 0) ? 64 : 32;
+  cuuint64_t dims[4] = {(cuuint64_t)p->D, (cuuint64_t)p->H, (cuuint64_t)p->S, (cuuint64_t)p->B};
+  cuuint64_t strides[3] = {(cuuint64_t)p->S * p->D * 2, (cuuint64_t)p->D * 2,
+                           (cuuint64_t)p->H * p->S * p->D * 2};
+  cuuint32_t box[4] = {(cuuint32_t)KC, (cuuint32_t)p->H, (cuuint32_t)R, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUtensorMapSwizzle sw = (KC == 64) ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(q), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// k [B,W,D] bf16 as dims (D, W, B); box {KC, 128, 1}.  Entries past W read as zero.
+bool make_k_map(CUtensorMap* m, const csa_problem* p, const void* k) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const int KC = (p->D % 64 == 0) ? 64 : 32;
+  cuuint64_t dims[3] = {(cuuint64_t)p->D, (cuuint64_t)p->W, (cuuint64_t)p->B};
+  cuuint64_t strides[2] = {(cuuint64_t)p->D * 2, (cuuint64_t)p->W * p->D * 2};
+  cuuint32_t box[3] = {(cuuint32_t)KC, (cuuint32_t)kTileT, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  const CUtensorMapSwizzle sw = (KC == 64) ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(k), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+csa_status run_index_kernel(const csa_problem* p, bool fused, const void* q, const void* k, const void* w,
+                            const int32_t* q_seg, const int32_t* kv_seg, const int64_t* q_start, float* scores,
+                            int32_t* idx, cudaStream_t stream) {
+  const bool row_kernel = use_row_kernel(p);
+  KernelChoice kc{p->H, p->D, row_kernel ? 1 : 4, fused};
+  CUtensorMap tq, tk;
+  if (!make_q_map(&tq, p, q, kc.R) || !make_k_map(&tk, p, k)) return CSA_ERR_CUDA;
+  KParams kp;
+  std::memset(&kp, 0, sizeof(kp));
+  kp.B = p->B;
+  kp.S = p->S;
+  kp.W = p->W;
+  kp.r = p->compress_rate;
+  kp.K = p->top_k;
+  kp.scale = p->scale;
+  kp.w_f32 = (p->w_dtype == CSA_F32) ? 1 : 0;
+  kp.w = w;
+  kp.q_seg = q_seg;
+  kp.kv_seg = kv_seg;
+  kp.q_start = q_start;
+  kp.scores = scores;
+  kp.idx = idx;
+  kp.n_rb = (p->S + kc.R - 1) / kc.R;
+  kp.n_tiles = (p->W + kTileT - 1) / kTileT;
+  kp.chunk_tiles = row_kernel ? std::min(kp.n_tiles, kDecodeChunkTiles) : kp.n_tiles;
+  kp.n_chunks = (kp.n_tiles + kp.chunk_tiles - 1) / kp.chunk_tiles;
+  const long long items = (long long)p->B * kp.n_rb * kp.n_chunks;
+  if (items > 0x7FFFFFFFll) return CSA_ERR_UNSUPPORTED;
+  kp.n_items = (int)items;
+  kp.w_pad = kp.n_tiles * kTileT;
+  kp.wait_ns = kWaitNs;
+  if (index_kernel_smem(kc, kp.w_pad) == 0) return CSA_ERR_UNSUPPORTED;
+  if (index_kernel_smem(kc, kp.w_pad) > 227u * 1024u) return CSA_ERR_UNSUPPORTED;
+  const int sms = num_sms();
+  if (sms <= 0) return CSA_ERR_CUDA;
+  const int grid = (int)std::min<long long>(items, sms);
+  if (launch_index_kernel(kc, tq, tk, kp, grid, stream) != cudaSuccess) return CSA_ERR_CUDA;
+  return CSA_OK;
+}
+
+size_t fused_workspace_bytes(const csa_problem* p) {
+  if (check_problem(p) != CSA_OK || fused_in_smem(p)) return 0;
+  return (size_t)p->B * p->S * p->W * sizeof(float);
+}
+
+}  // namespace
+}  // namespace csa
+
+using namespace csa;
+
+extern "C" {
+
+csa_status csa_index_score(const csa_problem* p, const void* q, const void* k, const void* w,
+                           const int32_t* q_seg, const int32_t* kv_seg, const int64_t* q_start, float* scores,
+                           void* stream) {
+  csa_status st = check_problem(p);
+  if (st != CSA_OK) return st;
+  if ((st = check_inputs(p, q, k, w, q_seg, kv_seg, q_start)) != CSA_OK) return st;
+  if (scores == nullptr || !aligned(scores, 4)) return CSA_ERR_INVALID_ARG;
+  if (!shape_supported(p)) return CSA_ERR_UNSUPPORTED;
+  return run_index_kernel(p, false, q, k, w, q_seg, kv_seg, q_start, scores, nullptr,
+                          static_cast<cudaStream_t>(stream));
+}
+
+csa_status csa_index_topk(const csa_problem* p, const float* scores, int32_t* idx, void* workspace,
+                          size_t workspace_bytes, void* stream) {
+  (void)workspace;
+  (void)workspace_bytes;
+  csa_status st = check_problem(p);
+  if (st != CSA_OK) return st;
+  if (scores == nullptr || idx == nullptr || !aligned(scores, 4) || !aligned(idx, 4)) return CSA_ERR_INVALID_ARG;
+  if (p->W > kTopkMaxW) return CSA_ERR_UNSUPPORTED;
+  const long long rows = (long long)p->B * p->S;
+  if (launch_topk(scores, idx, rows, p->W, p->top_k, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return CSA_ERR_CUDA;
+  return CSA_OK;
+}
+
+csa_status csa_index_fused(const csa_problem* p, const void* q, const void* k, const void* w,
+                           const int32_t* q_seg, const int32_t* kv_seg, const int64_t* q_start, int32_t* idx,
+                           float* scores_dbg, void* workspace, size_t workspace_bytes, void* stream) {
+  csa_status st = check_problem(p);
+  if (st != CSA_OK) return st;
+  if ((st = check_inputs(p, q, k, w, q_seg, kv_seg, q_start)) != CSA_OK) return st;
+  if (idx == nullptr || !aligned(idx, 4)) return CSA_ERR_INVALID_ARG;
+  if (scores_dbg != nullptr && !aligned(scores_dbg, 4)) return CSA_ERR_INVALID_ARG;
+  if (!shape_supported(p)) return CSA_ERR_UNSUPPORTED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (fused_in_smem(p)) return run_index_kernel(p, true, q, k, w, q_seg, kv_seg, q_start, scores_dbg, idx, s);
+  // Large W: scores pass through the caller's workspace, then a selection pass.
+  if (p->W > kTopkMaxW) return CSA_ERR_UNSUPPORTED;
+  const size_t need = fused_workspace_bytes(p);
+  float* sc = scores_dbg;
+  if (sc == nullptr) {
+    if (workspace == nullptr || workspace_bytes < need) return CSA_ERR_INVALID_ARG;
+    if (!aligned(workspace, 16)) return CSA_ERR_INVALID_ARG;
+    sc = static_cast<float*>(workspace);
+  }
+  st = run_index_kernel(p, false, q, k, w, q_seg, kv_seg, q_start, sc, nullptr, s);
+  if (st != CSA_OK) return st;
+  if (launch_topk(sc, idx, (long long)p->B * p->S, p->W, p->top_k, s) != cudaSuccess) return CSA_ERR_CUDA;
+  return CSA_OK;
+}
+
+size_t csa_index_workspace_size(const csa_problem* p, int32_t which) {
+  if (which == 1) return fused_workspace_bytes(p);
+  return 0;
+}
+
+csa_status csa_index_device_status(void* stream) {
+  uint32_t a = 0, b = 0;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (take_status_prefill(&a, s) != cudaSuccess) return CSA_ERR_CUDA;
+  if (take_status_other(&b, s) != cudaSuccess) return CSA_ERR_CUDA;
+  const uint32_t v = a | b;
+  if (v & kErrTimeout) return CSA_ERR_TIMEOUT;
+  if (v != 0u) return CSA_ERR_DEVICE;
+  return CSA_OK;
+}
+
+csa_status csa_index_selftest_timeout(uint32_t timeout_us, void* stream) {
+  if (timeout_us == 0 || timeout_us > 10000000u) return CSA_ERR_INVALID_ARG;
+  if (launch_selftest_timeout((unsigned long long)timeout_us * 1000ull, static_cast<cudaStream_t>(stream)) !=
+      cudaSuccess)
+    return CSA_ERR_CUDA;
+  return CSA_OK;
+}
+
+const char* csa_status_string(csa_status s) {
+  switch (s) {
+    case CSA_OK: return "ok";
+    case CSA_ERR_INVALID_ARG: return "invalid argument";
+    case CSA_ERR_UNSUPPORTED: return "unsupported problem shape";
+    case CSA_ERR_CUDA: return "CUDA call or launch failed";
+    case CSA_ERR_TIMEOUT: return "a bounded device wait gave up";
+    case CSA_ERR_DEVICE: return "device-side error";
+  }
+  return "unknown status";
+}
+
+int32_t csa_index_abi_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,543 @@
+// csa_score_kernel.cuh -- the persistent, warp-specialised indexer kernel.
+//
+// One CTA per SM walks a static list of work items.  An item is R query rows
+// of one batch (all H heads) and a range of compressed-entry tiles of 128.
+// Per item the tensor cores compute, for every tile,
+//     acc[t, (j,h)] = sum_d k[b,t,d] * q[b,h,s0+j,d]        (tcgen05 UMMA)
+// with the k tile as operand A (M = 128 entries) and the item's q block as
+// operand B (N = R*H columns ordered j*H + h), accumulating in TMEM.  The
+// epilogue warps read their lane's row of the accumulator, so each thread
+// owns one entry t and reduces over heads in registers:
+//     score[s0+j, t] = scale * sum_h w[s0+j,h] * max(acc[t,(j,h)], 0)
+// (ReLU(scale*x) = scale*ReLU(x) because scale > 0), then apply the future
+// and segment masks.  This is the head-reduced score of "Add StreamIndex
+// Kernel for CSA [Deepseek v4]" (Description; head-chunked on-chip
+// accumulation instead of the [B,H,S,W] tensor) with the masks of "DSV4: Add
+// indexer_save_selection and indexer_sharded_topk" (mask review hunk).
+//
+// Warp roles (block = 4 control warps + EW epilogue warps):
+//   warp 0  TMA producer: q block per item, k tiles into a ring of stages
+//   warp 1  TMEM owner and UMMA issuer (one elected thread)
+//   warp 2  scheduler: per item computes the visible tile range, per-row
+//           thresholds / segment ids / visible counts and stages the
+//           weights into a ring of item slots
+//   warp 3  idle
+//   warps 4..4+EW-1  epilogue (warp w reads TMEM lanes 32*(w%4) ..)
+// FUSED: scores stay in shared memory ([R][W] fp32) and the epilogue warps
+// then run the per-row selection, two warps per row.
+//
+// Tiles wholly past the rows' future-mask bound, or (with segment ids)
+// outside the range of entries sharing a segment with the item's rows, are
+// never loaded or multiplied.  Every mbarrier wait is bounded.
+#pragma once
+
+#include "csa_ptx.cuh"
+#include "csa_select.cuh"
+
+namespace csa {
+
+constexpr int kTileT = 128;  // compressed entries per tile (UMMA M)
+constexpr int kSlots = 4;    // item ring depth
+
+struct KParams {
+  int B, S, W, r, K;
+  float scale;
+  int w_f32;
+  const void* w;
+  const int32_t* q_seg;
+  const int32_t* kv_seg;
+  const int64_t* q_start;
+  float* scores;  // score mode: output; fused: optional debug copy
+  int32_t* idx;   // fused: selection output
+  int n_rb, n_tiles, n_chunks, chunk_tiles, n_items;
+  int w_pad;  // fused: row pitch (floats) of the shared score rows
+  unsigned long long wait_ns;
+};
+
+template <int R>
+struct ItemDesc {
+  int b, s0;
+  int t_lo, t_hi;  // tiles computed: [t_lo, t_hi)
+  int c_lo, c_hi;  // tiles owned by the item: [c_lo, c_hi)
+  int trivial;     // fused: every row keeps all its visible entries, no scores needed
+  int thr[R];      // rows' visible bound min(W, (pos+1)/r); 0 for rows past S
+  int seg[R];
+  int nvis[R];
+};
+
+constexpr uint32_t pow2_cols(uint32_t n) {
+  uint32_t c = 32;
+  while (c < n) c <<= 1;
+  return c;
+}
+
+template <int H_, int D_, int R_, bool FUSED_>
+struct Cfg {
+  static constexpr int H = H_, D = D_, R = R_;
+  static constexpr bool FUSED = FUSED_;
+  static constexpr int N = R * H;
+  static_assert(N % 16 == 0 && N >= 16 && N <= 256, "UMMA N must be 16..256 in steps of 16");
+  static constexpr int KC = (D % 64 == 0) ? 64 : 32;  // K elements per swizzled row
+  static constexpr int ROWB = KC * 2;                  // 128 B (SW128) or 64 B (SW64)
+  static constexpr int NKC = D / KC;
+  static_assert(D % 32 == 0, "head dim must be a multiple of 32");
+  static constexpr int KSTAGES = (R == 1) ? 5 : 2;
+  static constexpr int QBUF = FUSED ? 1 : 2;
+  static constexpr int EW = (R >= 2) ? 8 : 4;  // epilogue warps
+  static constexpr int RW = (R >= 2) ? R / 2 : 1;  // rows per epilogue warp
+  static_assert(R == 1 || R % 2 == 0, "R must be 1 or even");
+  static constexpr int NTHREADS = 128 + EW * 32;
+  static constexpr uint32_t QCHUNK = N * ROWB;        // bytes of one K-chunk of the q block
+  static constexpr uint32_t KCHUNK = kTileT * ROWB;   // bytes of one K-chunk of a k tile
+  static constexpr uint32_t QBYTES = QCHUNK * NKC;
+  static constexpr uint32_t KBYTES = KCHUNK * NKC;
+  static constexpr uint32_t TMEM_COLS = pow2_cols(2 * N);
+  static constexpr uint32_t IDESC = idesc_bf16_f32(kTileT, N);
+  // shared memory layout (offsets from a 1024-aligned base)
+  static constexpr uint32_t OFF_Q = 0;
+  static constexpr uint32_t OFF_K = (OFF_Q + QBUF * QBYTES + 1023) & ~1023u;
+  static constexpr uint32_t OFF_W = (OFF_K + KSTAGES * KBYTES + 1023) & ~1023u;
+  static constexpr uint32_t OFF_DESC = OFF_W + kSlots * R * H * 4;
+  static constexpr uint32_t OFF_BAR = (OFF_DESC + kSlots * sizeof(ItemDesc<R>) + 15) & ~15u;
+  // barriers: item_full[S], item_empty[S], q_full[QB], q_empty[QB], k_full[KS], k_empty[KS],
+  //           acc_full[2], acc_empty[2], drain
+  static constexpr int NBAR = 2 * kSlots + 2 * QBUF + 2 * KSTAGES + 4 + 1;
+  static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;  // tmem base, abort flag
+  static constexpr uint32_t OFF_SCR = (OFF_MISC + 16 + 15) & ~15u;
+  static constexpr uint32_t NSCR = FUSED ? R : 0;
+  static constexpr uint32_t OFF_SROW = (OFF_SCR + NSCR * sizeof(SelectScratch) + 127) & ~127u;
+  // dynamic shared memory for a given fused row pitch (+1 KB alignment slack)
+  static constexpr uint32_t smem_bytes(int w_pad) {
+    return OFF_SROW + (FUSED ? (uint32_t)R * (uint32_t)w_pad * 4u : 0u) + 1024u;
+  }
+};
+
+template <class C>
+struct Smem {
+  uint8_t* base;
+  __device__ uint8_t* q(int i) const { return base + C::OFF_Q + i * C::QBYTES; }
+  __device__ uint8_t* k(int i) const { return base + C::OFF_K + i * C::KBYTES; }
+  __device__ float* w(int slot) const { return reinterpret_cast<float*>(base + C::OFF_W) + slot * C::R * C::H; }
+  __device__ ItemDesc<C::R>* desc(int slot) const {
+    return reinterpret_cast<ItemDesc<C::R>*>(base + C::OFF_DESC) + slot;
+  }
+  __device__ uint64_t* bar(int i) const { return reinterpret_cast<uint64_t*>(base + C::OFF_BAR) + i; }
+  __device__ uint64_t* item_full(int s) const { return bar(s); }
+  __device__ uint64_t* item_empty(int s) const { return bar(kSlots + s); }
+  __device__ uint64_t* q_full(int i) const { return bar(2 * kSlots + i); }
+  __device__ uint64_t* q_empty(int i) const { return bar(2 * kSlots + C::QBUF + i); }
+  __device__ uint64_t* k_full(int i) const { return bar(2 * kSlots + 2 * C::QBUF + i); }
+  __device__ uint64_t* k_empty(int i) const { return bar(2 * kSlots + 2 * C::QBUF + C::KSTAGES + i); }
+  __device__ uint64_t* acc_full(int i) const { return bar(2 * kSlots + 2 * C::QBUF + 2 * C::KSTAGES + i); }
+  __device__ uint64_t* acc_empty(int i) const { return bar(2 * kSlots + 2 * C::QBUF + 2 * C::KSTAGES + 2 + i); }
+  __device__ uint64_t* drain() const { return bar(2 * kSlots + 2 * C::QBUF + 2 * C::KSTAGES + 4); }
+  __device__ uint32_t* tmem_slot() const { return reinterpret_cast<uint32_t*>(base + C::OFF_MISC); }
+  __device__ volatile uint32_t* abort_flag() const {
+    return reinterpret_cast<volatile uint32_t*>(base + C::OFF_MISC + 4);
+  }
+  __device__ SelectScratch* scratch(int j) const {
+    return reinterpret_cast<SelectScratch*>(base + C::OFF_SCR) + j;
+  }
+  __device__ float* srow(int j, int w_pad) const {
+    return reinterpret_cast<float*>(base + C::OFF_SROW) + (size_t)j * w_pad;
+  }
+};
+
+// Item index -> (b, row block, chunk).  Row blocks run from the last (most
+// visible entries, most work) to the first so the static round-robin
+// assignment of items to CTAs stays balanced under the causal mask.
+__device__ __forceinline__ void item_coords(const KParams& p, int item, int& b, int& rb, int& c) {
+  c = item % p.n_chunks;
+  const int rest = item / p.n_chunks;
+  b = rest % p.B;
+  rb = p.n_rb - 1 - rest / p.B;
+}
+
+template <class C>
+__device__ void run_scheduler(const KParams& p, const Smem<C>& sm, const WaitCtl& ctl) {
+  constexpr int R = C::R, H = C::H;
+  const uint32_t lane = lane_id();
+  const bool segs = p.q_seg != nullptr;
+  int it = 0;
+  for (int item = blockIdx.x; item < p.n_items; item += gridDim.x, ++it) {
+    const int slot = it % kSlots;
+    mbar_wait(sm.item_empty(slot), ((it / kSlots) & 1) ^ 1, ctl);
+    int b, rb, c;
+    item_coords(p, item, b, rb, c);
+    const int s0 = rb * R;
+    const long long qs0 = p.q_start ? (long long)p.q_start[b] : 0ll;
+    int thr[R], seg[R], nvis[R];
+    int thr_max = 0;
+#pragma unroll
+    for (int j = 0; j < R; ++j) {
+      const int s = s0 + j;
+      long long tv = 0;
+      if (s < p.S) {
+        tv = (qs0 + s + 1) / p.r;
+        tv = tv < 0 ? 0 : (tv > p.W ? p.W : tv);
+      }
+      thr[j] = (int)tv;
+      seg[j] = (segs && s < p.S) ? p.q_seg[(size_t)b * p.S + s] : 0;
+      thr_max = max(thr_max, thr[j]);
+    }
+    const int c_lo = c * p.chunk_tiles;
+    const int c_hi = min(p.n_tiles, c_lo + p.chunk_tiles);
+    int t_lo = c_lo, t_hi = c_lo;
+    if (!segs) {
+#pragma unroll
+      for (int j = 0; j < R; ++j) nvis[j] = max(0, min(thr[j], c_hi * kTileT) - c_lo * kTileT);
+      t_hi = max(c_lo, min(c_hi, (thr_max + kTileT - 1) / kTileT));
+    } else {
+      int cnt[R];
+#pragma unroll
+      for (int j = 0; j < R; ++j) cnt[j] = 0;
+      int tmin = 0x7FFFFFFF, tmax = -1;
+      const int e_hi = min(c_hi * kTileT, thr_max);
+      const int32_t* kv = p.kv_seg + (size_t)b * p.W;
+      for (int t = c_lo * kTileT + (int)lane; t < e_hi; t += 32) {
+        const int ks = kv[t];
+        bool any = false;
+#pragma unroll
+        for (int j = 0; j < R; ++j) {
+          const bool m = (t < thr[j]) && (ks == seg[j]);
+          cnt[j] += m;
+          any |= m;
+        }
+        if (any) {
+          tmin = min(tmin, t);
+          tmax = max(tmax, t);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < R; ++j) nvis[j] = (int)__reduce_add_sync(0xFFFFFFFFu, (unsigned)cnt[j]);
+      tmin = __reduce_min_sync(0xFFFFFFFFu, tmin);
+      tmax = __reduce_max_sync(0xFFFFFFFFu, tmax);
+      if (tmax >= 0) {
+        t_lo = tmin / kTileT;
+        t_hi = tmax / kTileT + 1;
+      }
+    }
+    int trivial = 0;
+    if (C::FUSED && p.scores == nullptr) {
+      trivial = 1;
+#pragma unroll
+      for (int j = 0; j < R; ++j) trivial &= (nvis[j] <= p.K) ? 1 : 0;
+      if (trivial) t_hi = t_lo;
+    }
+    // stage the weights (fp32) of the item's rows; rows past S get 0
+    float* ws = sm.w(slot);
+    for (int i = (int)lane; i < R * H; i += 32) {
+      const int j = i / H, h = i % H;
+      const int s = s0 + j;
+      float v = 0.f;
+      if (s < p.S) {
+        const size_t off = ((size_t)b * p.S + s) * H + h;
+        v = p.w_f32 ? reinterpret_cast<const float*>(p.w)[off]
+                    : __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p.w)[off]);
+      }
+      ws[i] = v;
+    }
+    if (lane == 0) {
+      ItemDesc<R>* d = sm.desc(slot);
+      d->b = b;
+      d->s0 = s0;
+      d->t_lo = t_lo;
+      d->t_hi = t_hi;
+      d->c_lo = c_lo;
+      d->c_hi = c_hi;
+      d->trivial = trivial;
+#pragma unroll
+      for (int j = 0; j < R; ++j) {
+        d->thr[j] = thr[j];
+        d->seg[j] = seg[j];
+        d->nvis[j] = nvis[j];
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(sm.item_full(slot));
+  }
+}
+
+template <class C>
+__device__ void run_producer(const KParams& p, const Smem<C>& sm, const WaitCtl& ctl, const CUtensorMap* tq,
+                             const CUtensorMap* tk) {
+  uint32_t kcount = 0, qcount = 0;
+  int it = 0;
+  for (int item = blockIdx.x; item < p.n_items; item += gridDim.x, ++it) {
+    const int slot = it % kSlots;
+    const bool ok_item = mbar_wait(sm.item_full(slot), (it / kSlots) & 1, ctl);
+    const ItemDesc<C::R>* d = sm.desc(slot);
+    const int b = d->b, s0 = d->s0, t_lo = d->t_lo, t_hi = d->t_hi;
+    mbar_arrive(sm.item_empty(slot));
+    if (!ok_item || t_hi <= t_lo) continue;
+    const int qb = qcount % C::QBUF;
+    if (mbar_wait(sm.q_empty(qb), ((qcount / C::QBUF) & 1) ^ 1, ctl)) {
+      mbar_arrive_expect_tx(sm.q_full(qb), C::QBYTES);
+#pragma unroll
+      for (int c = 0; c < C::NKC; ++c)
+        tma_load_4d(sm.q(qb) + c * C::QCHUNK, tq, sm.q_full(qb), c * C::KC, 0, s0, b);
+    }
+    ++qcount;
+    for (int tile = t_lo; tile < t_hi; ++tile) {
+      const int st = kcount % C::KSTAGES;
+      if (mbar_wait(sm.k_empty(st), ((kcount / C::KSTAGES) & 1) ^ 1, ctl)) {
+        mbar_arrive_expect_tx(sm.k_full(st), C::KBYTES);
+#pragma unroll
+        for (int c = 0; c < C::NKC; ++c)
+          tma_load_3d(sm.k(st) + c * C::KCHUNK, tk, sm.k_full(st), c * C::KC, tile * kTileT, b);
+      }
+      ++kcount;
+    }
+  }
+  // make sure no copy is still landing in shared memory when the CTA exits
+  WaitCtl drain_ctl{ctl.abort_flag, ctl.limit_ns};
+  volatile uint32_t dummy = 0;
+  drain_ctl.abort_flag = &dummy;
+  for (uint32_t i = 0; i < C::KSTAGES && i < kcount; ++i) {
+    const uint32_t last = kcount - 1 - i;  // most recent use of stage last % KSTAGES
+    mbar_wait(sm.k_full(last % C::KSTAGES), (last / C::KSTAGES) & 1, drain_ctl);
+  }
+  for (uint32_t i = 0; i < C::QBUF && i < qcount; ++i) {
+    const uint32_t last = qcount - 1 - i;
+    mbar_wait(sm.q_full(last % C::QBUF), (last / C::QBUF) & 1, drain_ctl);
+  }
+}
+
+template <class C>
+__device__ void run_mma(const KParams& p, const Smem<C>& sm, const WaitCtl& ctl, uint32_t tmem_base) {
+  uint32_t kcount = 0, qcount = 0, acount = 0;
+  int it = 0;
+  for (int item = blockIdx.x; item < p.n_items; item += gridDim.x, ++it) {
+    const int slot = it % kSlots;
+    const bool ok_item = mbar_wait(sm.item_full(slot), (it / kSlots) & 1, ctl);
+    const ItemDesc<C::R>* d = sm.desc(slot);
+    const int t_lo = d->t_lo, t_hi = d->t_hi;
+    mbar_arrive(sm.item_empty(slot));
+    if (!ok_item || t_hi <= t_lo) continue;
+    const int qb = qcount % C::QBUF;
+    const bool q_ok = mbar_wait(sm.q_full(qb), (qcount / C::QBUF) & 1, ctl);
+    tc_fence_after();
+    const uint32_t q_addr = smem_u32(sm.q(qb));
+    for (int tile = t_lo; tile < t_hi; ++tile) {
+      const int st = kcount % C::KSTAGES;
+      const int a = acount & 1;
+      const bool k_ok = mbar_wait(sm.k_full(st), (kcount / C::KSTAGES) & 1, ctl);
+      const bool a_ok = mbar_wait(sm.acc_empty(a), ((acount >> 1) & 1) ^ 1, ctl);
+      tc_fence_after();
+      if (q_ok && k_ok && a_ok) {
+        const uint32_t k_addr = smem_u32(sm.k(st));
+        const uint32_t d_tmem = tmem_base + (uint32_t)(a * C::N);
+#pragma unroll
+        for (int c = 0; c < C::NKC; ++c) {
+#pragma unroll
+          for (int kk = 0; kk < C::KC / 16; ++kk) {
+            const uint64_t adesc = smem_desc_kmajor(k_addr + c * C::KCHUNK + kk * 32, C::ROWB);
+            const uint64_t bdesc = smem_desc_kmajor(q_addr + c * C::QCHUNK + kk * 32, C::ROWB);
+            umma_bf16(d_tmem, adesc, bdesc, C::IDESC, (c | kk) != 0 ? 1u : 0u);
+          }
+        }
+      }
+      umma_commit(sm.k_empty(st));
+      umma_commit(sm.acc_full(a));
+      ++kcount;
+      ++acount;
+    }
+    umma_commit(sm.q_empty(qb));
+    ++qcount;
+  }
+  // every MMA issued above has completed once this barrier fires
+  umma_commit(sm.drain());
+  volatile uint32_t dummy = 0;
+  WaitCtl drain_ctl{&dummy, ctl.limit_ns};
+  mbar_wait(sm.drain(), 0, drain_ctl);
+}
+
+// Accumulate this warp's rows over heads from one TMEM accumulator buffer.
+template <class C>
+__device__ __forceinline__ void epilogue_accumulate(uint32_t t_row, const float* ws, int hf,
+                                                    float (&acc)[C::RW]) {
+  constexpr int H = C::H, RW = C::RW;
+#pragma unroll
+  for (int jj = 0; jj < RW; ++jj) acc[jj] = 0.f;
+  if constexpr (H % 32 == 0) {
+#pragma unroll
+    for (int jj = 0; jj < RW; ++jj) {
+      const int j = hf * RW + jj;
+      float2 a2 = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int hc = 0; hc < H / 32; ++hc) {
+        float v[32];
+        tmem_ld32(t_row + (uint32_t)(j * H + hc * 32), v);
+        const float2* w2 = reinterpret_cast<const float2*>(ws + j * H + hc * 32);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float2 r2 = make_float2(fmaxf(v[2 * i], 0.f), fmaxf(v[2 * i + 1], 0.f));
+          a2 = ffma2(w2[i], r2, a2);
+        }
+      }
+      acc[jj] = a2.x + a2.y;
+    }
+  } else {
+    static_assert((C::RW * H) % 8 == 0, "small-head path loads 8 columns at a time");
+#pragma unroll
+    for (int c0 = 0; c0 < RW * H; c0 += 8) {
+      float v[8];
+      tmem_ld8(t_row + (uint32_t)(hf * RW * H + c0), v);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int col = c0 + i;
+        const int jj = col / H, h = col % H;
+        acc[jj] = fmaf(ws[(hf * RW + jj) * H + h], fmaxf(v[i], 0.f), acc[jj]);
+      }
+    }
+  }
+}
+
+template <class C>
+__device__ void run_epilogue(const KParams& p, const Smem<C>& sm, const WaitCtl& ctl, uint32_t tmem_base,
+                             int e /* epilogue warp 0..EW-1 */) {
+  constexpr int R = C::R, RW = C::RW;
+  const uint32_t lane = lane_id();
+  const int quarter = (4 + e) % 4;  // warp id % 4 selects the TMEM lane quarter
+  const int hf = (C::EW == 8) ? (e / 4) : 0;
+  const bool segs = p.q_seg != nullptr;
+  const uint32_t t_lane = tmem_base + ((uint32_t)(quarter * 32) << 16);
+  uint32_t acount = 0;
+  int it = 0;
+  for (int item = blockIdx.x; item < p.n_items; item += gridDim.x, ++it) {
+    const int slot = it % kSlots;
+    mbar_wait(sm.item_full(slot), (it / kSlots) & 1, ctl);
+    const ItemDesc<R>* d = sm.desc(slot);
+    const int b = d->b, s0 = d->s0, t_lo = d->t_lo, t_hi = d->t_hi, c_lo = d->c_lo, c_hi = d->c_hi;
+    const int trivial = d->trivial;
+    int thr[RW], seg[RW];
+#pragma unroll
+    for (int jj = 0; jj < RW; ++jj) {
+      thr[jj] = d->thr[hf * RW + jj];
+      seg[jj] = d->seg[hf * RW + jj];
+    }
+    const float* ws = sm.w(slot);
+    const bool write_all = !C::FUSED || p.scores != nullptr;
+    const int tile_begin = write_all ? c_lo : t_lo;
+    const int tile_end = write_all ? c_hi : t_hi;
+    for (int tile = tile_begin; tile < tile_end; ++tile) {
+      const bool computed = tile >= t_lo && tile < t_hi;
+      const int t = tile * kTileT + quarter * 32 + (int)lane;
+      float acc[RW];
+#pragma unroll
+      for (int jj = 0; jj < RW; ++jj) acc[jj] = 0.f;
+      if (computed) {
+        const int a = acount & 1;
+        const bool ok = mbar_wait(sm.acc_full(a), (acount >> 1) & 1, ctl);
+        tc_fence_after();
+        if (ok) epilogue_accumulate<C>(t_lane + (uint32_t)(a * C::N), ws, hf, acc);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(sm.acc_empty(a));
+        ++acount;
+      }
+      int kvs = 0;
+      if (segs && computed && t < p.W) kvs = p.kv_seg[(size_t)b * p.W + t];
+#pragma unroll
+      for (int jj = 0; jj < RW; ++jj) {
+        const int j = hf * RW + jj;
+        const int s = s0 + j;
+        const bool vis = computed && t < thr[jj] && (!segs || kvs == seg[jj]);
+        const float val = vis ? p.scale * acc[jj] : -INFINITY;
+        if constexpr (C::FUSED) {
+          if (t < p.w_pad) sm.srow(j, p.w_pad)[t] = val;
+        }
+        if (p.scores != nullptr && s < p.S && t < p.W) p.scores[((size_t)b * p.S + s) * p.W + t] = val;
+      }
+    }
+    if constexpr (C::FUSED) {
+      named_bar_sync(1, C::EW * 32);  // the item's scores are in shared memory
+      const int j = e / 2;            // two warps per row
+      const int s = s0 + j;
+      Team<64> team{(uint32_t)(2 + j), (uint32_t)((e & 1) * 32) + lane};
+      if (j < R && s < p.S) {
+        int32_t* out = p.idx + ((size_t)b * p.S + s) * p.K;
+        const int thr_j = d->thr[j];
+        const int seg_j = d->seg[j];
+        if (trivial) {
+          if (!segs) {
+            for (int i = (int)team.tid; i < p.K; i += 64) out[i] = (i < thr_j) ? i : -1;
+          } else {
+            const int32_t* kv = p.kv_seg + (size_t)b * p.W;
+            team_write_ordered<64>(0, thr_j, 0u, (uint32_t)p.K, out, sm.scratch(j), team,
+                                   [&](int tt) -> int { return (kv[tt] == seg_j) ? 1 : 0; });
+          }
+        } else {
+          const int e_lo = t_lo * kTileT;
+          const int e_hi = min(t_hi * kTileT, p.W);
+          team_topk_row<64>(sm.srow(j, p.w_pad), e_lo, e_hi, (uint32_t)p.K, out, sm.scratch(j), team);
+        }
+      }
+      named_bar_sync(1, C::EW * 32);  // shared score rows may be overwritten
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(sm.item_empty(slot));
+  }
+}
+
+template <class C>
+__global__ void __launch_bounds__(C::NTHREADS, 1)
+    csa_index_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
+                     const KParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  Smem<C> sm{base};
+  const int warp = threadIdx.x / 32;
+  const uint32_t lane = lane_id();
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kSlots; ++s) {
+      mbar_init(sm.item_full(s), 1);
+      mbar_init(sm.item_empty(s), 2 + C::EW);
+    }
+    for (int i = 0; i < C::QBUF; ++i) {
+      mbar_init(sm.q_full(i), 1);
+      mbar_init(sm.q_empty(i), 1);
+    }
+    for (int i = 0; i < C::KSTAGES; ++i) {
+      mbar_init(sm.k_full(i), 1);
+      mbar_init(sm.k_empty(i), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(sm.acc_full(i), 1);
+      mbar_init(sm.acc_empty(i), C::EW);
+    }
+    mbar_init(sm.drain(), 1);
+    *sm.abort_flag() = 0u;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmap_q);
+    prefetch_tmap(&tmap_k);
+  }
+  if (warp == 1) {
+    tmem_alloc(sm.tmem_slot(), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *sm.tmem_slot();
+  const WaitCtl ctl{sm.abort_flag(), p.wait_ns};
+
+  if (warp == 0) {
+    if (lane == 0) run_producer<C>(p, sm, ctl, &tmap_q, &tmap_k);
+  } else if (warp == 1) {
+    if (lane == 0) run_mma<C>(p, sm, ctl, tmem_base);
+  } else if (warp == 2) {
+    run_scheduler<C>(p, sm, ctl);
+  } else if (warp >= 4) {
+    run_epilogue<C>(p, sm, ctl, tmem_base, warp - 4);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, C::TMEM_COLS);
+}
+
+}  // namespace csa

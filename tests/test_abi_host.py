@@ -1,0 +1,109 @@
+"""Host-side checks of the C-ABI library (no GPU, no compute calls).
+
+The library must load, export every entry point declared in
+include/csa_index.h, and reject bad arguments on the host before any CUDA
+call is made.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import sparse_attention_indexer_csa_gb300 as csa
+from sparse_attention_indexer_csa_gb300 import abi
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(abi.LIB_PATH):
+        from sparse_attention_indexer_csa_gb300 import build
+        build.build()
+    return abi.load()
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "csa_index.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(csa_[a-z_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared()
+    assert "csa_index_score" in names and "csa_index_fused" in names and "csa_index_topk" in names
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(abi.EXPORTED)
+
+
+def test_abi_version_and_strings(lib):
+    assert lib.csa_index_abi_version() == 100
+    for s in range(6):
+        assert abi.status_string(s)
+    assert abi.status_string(99) == "unknown status"
+
+
+def _p(**kw):
+    d = dict(B=1, H=64, S=16, D=128, W=4, compress_rate=4, scale=0.1, top_k=2, w_dtype=abi.CSA_BF16)
+    d.update(kw)
+    return abi.Problem(**d)
+
+
+FAKE = ctypes.c_void_p(0x10000)  # 16-byte aligned, never dereferenced by the checks
+ODD = ctypes.c_void_p(0x10002)
+
+
+def _score(lib, p, q=FAKE, k=FAKE, w=FAKE, qs=None, kvs=None, st=None, out=FAKE):
+    return lib.csa_index_score(ctypes.byref(p) if p is not None else None, q, k, w, qs, kvs, st, out, None)
+
+
+@pytest.mark.parametrize("bad", [dict(B=0), dict(H=0), dict(S=-1), dict(D=0), dict(W=0),
+                                 dict(compress_rate=0), dict(top_k=0), dict(scale=0.0),
+                                 dict(scale=-1.0), dict(scale=float("inf")), dict(scale=float("nan")),
+                                 dict(w_dtype=7)])
+def test_bad_problem_rejected(lib, bad):
+    assert _score(lib, _p(**bad)) == abi.CSA_ERR_INVALID_ARG
+
+
+def test_null_and_misaligned_pointers_rejected(lib):
+    assert _score(lib, None) == abi.CSA_ERR_INVALID_ARG
+    assert _score(lib, _p(), q=None) == abi.CSA_ERR_INVALID_ARG
+    assert _score(lib, _p(), out=None) == abi.CSA_ERR_INVALID_ARG
+    assert _score(lib, _p(), q=ODD) == abi.CSA_ERR_INVALID_ARG   # TMA needs 16-byte bases
+    assert _score(lib, _p(), k=ODD) == abi.CSA_ERR_INVALID_ARG
+    # segment ids must come in pairs
+    assert _score(lib, _p(), qs=FAKE) == abi.CSA_ERR_INVALID_ARG
+    assert _score(lib, _p(), kvs=FAKE) == abi.CSA_ERR_INVALID_ARG
+
+
+def test_unsupported_shapes_rejected_not_fallen_back(lib):
+    assert _score(lib, _p(H=32)) == abi.CSA_ERR_UNSUPPORTED
+    assert _score(lib, _p(D=64)) == abi.CSA_ERR_UNSUPPORTED
+    p = _p(W=60000)
+    assert lib.csa_index_topk(ctypes.byref(p), FAKE, FAKE, None, 0, None) == abi.CSA_ERR_UNSUPPORTED
+    p = _p(S=1, W=60000)
+    assert lib.csa_index_fused(ctypes.byref(p), FAKE, FAKE, FAKE, None, None, None, FAKE, None, None, 0,
+                               None) == abi.CSA_ERR_UNSUPPORTED
+
+
+def test_fused_large_w_needs_workspace(lib):
+    p = _p(S=1, W=32768, B=64)
+    need = abi.workspace_size(p, 1)
+    assert need == 64 * 1 * 32768 * 4
+    assert lib.csa_index_fused(ctypes.byref(p), FAKE, FAKE, FAKE, None, None, None, FAKE, None, None, 0,
+                               None) == abi.CSA_ERR_INVALID_ARG
+    assert abi.workspace_size(_p(W=4096, S=16384), 1) == 0  # scores stay on chip
+    assert abi.workspace_size(_p(), 0) == 0
+    assert abi.workspace_size(_p(B=0), 1) == 0
+
+
+def test_selftest_argument_checks(lib):
+    assert lib.csa_index_selftest_timeout(0, None) == abi.CSA_ERR_INVALID_ARG
+    assert lib.csa_index_selftest_timeout(20_000_000, None) == abi.CSA_ERR_INVALID_ARG
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    with pytest.raises(RuntimeError):
+        abi.load(str(tmp_path / "missing.so"))

@@ -1,0 +1,288 @@
+"""GPU parity of the CUDA path against the CPU oracle (through the C ABI)."""
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import sparse_attention_indexer_csa_gb300 as csa
+from csa_inputs import WORKLOADS, Inputs, Workload, make_inputs
+from oracle import csa_oracle as O
+from parity import (assert_status_ok, check_scores, check_select_exact, check_select_vs_oracle,
+                    gpu_fused, gpu_scores, oracle_scores, to_dev)
+
+pytestmark = pytest.mark.gpu
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    csa.load()
+    yield
+    assert_status_ok()
+
+
+# --------------------------------------------------------------------------- hand example
+@pytest.mark.parametrize("H,D", [(4, 32), (64, 128)])
+def test_hand_example_exact(H, D):
+    """The hand-worked case, zero-padded to a kernel's head count and head dim,
+    reproduces every score exactly and the selection (tie, padding, empty row)."""
+    g = json.load(open(os.path.join(GOLDEN, "hand_example.json")))
+    q = torch.zeros(1, H, 8, D)
+    q[0, :2, :, :2] = torch.tensor(g["q"], dtype=torch.float32)
+    k = torch.zeros(1, 4, D)
+    k[0, :, :2] = torch.tensor(g["k"], dtype=torch.float32)
+    w = torch.zeros(1, 8, H)
+    w[0, :, :2] = torch.tensor(g["w"], dtype=torch.float32)
+    dev = "cuda"
+    qd, kd, wd = q.to(torch.bfloat16).to(dev), k.to(torch.bfloat16).to(dev), w.to(dev)
+    sc = csa.index_score(qd, kd, wd, g["scale"], g["compress_rate"]).cpu().numpy()
+    exp = np.array([[float(v) for v in row] for row in g["expected_scores"]])
+    assert np.array_equal(sc[0], exp)
+    idx = csa.index_fused(qd, kd, wd, g["scale"], g["compress_rate"], g["top_k"])
+    assert idx[0].cpu().tolist() == g["expected_topk"]
+    idx2 = csa.index_topk(torch.from_numpy(sc).to(dev), g["top_k"])
+    assert idx2[0].cpu().tolist() == g["expected_topk"]
+    assert_status_ok()
+
+
+# --------------------------------------------------------------------------- full parity, small configs
+@pytest.mark.parametrize("name", ["tiny", "prefill_4k"])
+def test_full_parity(name):
+    wl = WORKLOADS[name]
+    inp = make_inputs(wl)
+    d = to_dev(inp)
+    ref = oracle_scores(inp)
+    gs = gpu_scores(inp, d)
+    idx_f, dbg = gpu_fused(inp, d, dbg=True)
+    idx_p, _ = gpu_fused(inp, d, dbg=False)
+    idx_t = csa.index_topk(gs, wl.top_k)
+    assert_status_ok()
+    g = gs.cpu().numpy()
+    check_scores(g, ref)
+    assert np.array_equal(dbg.cpu().numpy(), g), "fused debug scores differ from the score kernel"
+    gi = idx_p.cpu().numpy()
+    assert np.array_equal(idx_f.cpu().numpy(), gi)
+    assert np.array_equal(idx_t.cpu().numpy(), gi)
+    check_select_exact(g, gi, wl.top_k)
+    check_select_vs_oracle(ref, gi, wl.top_k)
+
+
+# --------------------------------------------------------------------------- full-size configs
+def _sample_rows(S, W, r, top_k, q_seg_row=None, n=1024, seed=0):
+    rng = np.random.default_rng(seed)
+    rows = set([0, 1, 2, 3, S - 1, S - 2, S // 2])
+    for s in range(S):  # rows around visible == top_k
+        if abs((s + 1) // r - top_k) <= 1:
+            rows.add(s)
+    if q_seg_row is not None:
+        cuts = np.nonzero(np.diff(q_seg_row))[0] + 1
+        for c in cuts:
+            for s in (c - 2, c - 1, c, c + 1, c + 4):
+                if 0 <= s < S:
+                    rows.add(int(s))
+    extra = rng.choice(S, size=max(0, n - len(rows)), replace=False)
+    rows.update(int(x) for x in extra)
+    return np.array(sorted(rows))[:max(n, len(rows))]
+
+
+@pytest.mark.parametrize("name", ["prefill_16k", "packed_8k"])
+def test_full_size_prefill(name):
+    """Fused path in the benchmarked launch configuration: selection checked on
+    every row against the oracle selector on the GPU scores, and on sampled rows
+    against the oracle's own scores."""
+    wl = WORKLOADS[name]
+    inp = make_inputs(wl)
+    d = to_dev(inp)
+    idx_p, _ = gpu_fused(inp, d, dbg=False)
+    gs = gpu_scores(inp, d)
+    assert_status_ok()
+    g = gs.cpu().numpy()
+    gi = idx_p.cpu().numpy()
+    del gs
+    check_select_exact(g, gi, wl.top_k)
+    for b in range(wl.B):
+        segrow = None if inp.q_seg is None else inp.q_seg[b].numpy()
+        rows = _sample_rows(wl.S, wl.W, wl.compress_rate, wl.top_k, segrow, n=1024, seed=b)
+        sub = Inputs(wl.with_(B=1), inp.q[b:b + 1], inp.k[b:b + 1], inp.w[b:b + 1],
+                     None if inp.q_seg is None else inp.q_seg[b:b + 1],
+                     None if inp.kv_seg is None else inp.kv_seg[b:b + 1],
+                     None if inp.q_start is None else inp.q_start[b:b + 1])
+        ref = oracle_scores(sub, rows=rows)
+        check_scores(g[b:b + 1, rows], ref)
+        check_select_vs_oracle(ref, gi[b:b + 1, rows], wl.top_k)
+
+
+def test_decode_full():
+    wl = WORKLOADS["decode_32k"]
+    inp = make_inputs(wl)
+    d = to_dev(inp)
+    idx_p, _ = gpu_fused(inp, d, dbg=False)
+    gs = gpu_scores(inp, d)
+    idx_t = csa.index_topk(gs, wl.top_k)
+    assert_status_ok()
+    g = gs.cpu().numpy()
+    gi = idx_p.cpu().numpy()
+    assert np.array_equal(idx_t.cpu().numpy(), gi)
+    ref = oracle_scores(inp)
+    check_scores(g, ref)
+    check_select_exact(g, gi, wl.top_k)
+    check_select_vs_oracle(ref, gi, wl.top_k)
+
+
+def test_decode_ignores_segment_ids():
+    wl = WORKLOADS["decode_32k"].with_(B=4, W=4096, q_start=16383)
+    inp = make_inputs(wl)
+    d = to_dev(inp)
+    seg_q = torch.zeros(wl.B, 1, dtype=torch.int32, device="cuda")
+    seg_k = torch.ones(wl.B, wl.W, dtype=torch.int32, device="cuda")  # would mask everything
+    a = csa.index_decode(d["q"], d["k"], d["w"], wl.scale, 4, wl.top_k, d["q_start"], seg_q, seg_k)
+    b = csa.index_fused(d["q"], d["k"], d["w"], wl.scale, 4, wl.top_k, q_start=d["q_start"])
+    assert torch.equal(a, b) and bool((a >= 0).all())
+
+
+# --------------------------------------------------------------------------- edge cases
+EDGE = [
+    # ragged W tail, S not a multiple of the 4-row block
+    dict(B=2, S=301, W=75, H=64, D=128, r=4, top_k=8),
+    # top_k larger than W (padding everywhere), single batch
+    dict(B=1, S=130, W=33, H=64, D=128, r=4, top_k=40),
+    # top_k = 1, compress rate 1 (W = S), bf16 weights
+    dict(B=1, S=200, W=200, H=64, D=128, r=1, top_k=1),
+    # start offsets: rows of a later slice of a longer sequence
+    dict(B=3, S=96, W=300, H=64, D=128, r=4, top_k=16, q_start=[1000, 0, 37]),
+    # W that spans several tiles plus a tail, small heads
+    dict(B=2, S=520, W=130, H=4, D=32, r=4, top_k=24),
+    # every row empty: start far before the first entry
+    dict(B=1, S=8, W=16, H=64, D=128, r=4, top_k=4, q_start=[-100]),
+    # W = 1
+    dict(B=2, S=9, W=1, H=4, D=32, r=4, top_k=3),
+    # two rows per sequence (row kernel) with ragged W
+    dict(B=5, S=2, W=1000, H=64, D=128, r=4, top_k=100, q_start=[3999, 4000, 100, 0, 5000]),
+]
+
+
+def _edge_inputs(c, seed=0, segs=None, w_dtype="bf16"):
+    wl = Workload(name="edge", B=c["B"], S=c["S"], W=c["W"], H=c["H"], D=c["D"], compress_rate=c["r"],
+                  top_k=c["top_k"], w_dtype=w_dtype, sigma_w=0.125, scale=c["D"] ** -0.5, seed=seed)
+    inp = make_inputs(wl)
+    if "q_start" in c:
+        inp.q_start = torch.tensor(c["q_start"], dtype=torch.int64)
+    if segs == "packed":
+        g = torch.Generator().manual_seed(seed + 7)
+        q_seg = torch.zeros(wl.B, wl.S, dtype=torch.int32)
+        for b in range(wl.B):
+            cuts = torch.sort(torch.randint(1, max(2, wl.S), (3,), generator=g)).values
+            for ct in cuts.tolist():
+                q_seg[b, ct:] += 1
+        last = (torch.arange(wl.W) * wl.compress_rate + wl.compress_rate - 1).clamp(max=wl.S - 1)
+        inp.q_seg = q_seg
+        inp.kv_seg = q_seg[:, last].contiguous()
+    elif segs == "scattered":  # arbitrary, non-contiguous ids
+        g = torch.Generator().manual_seed(seed + 9)
+        inp.q_seg = torch.randint(0, 3, (wl.B, wl.S), generator=g, dtype=torch.int32)
+        inp.kv_seg = torch.randint(0, 3, (wl.B, wl.W), generator=g, dtype=torch.int32)
+    return inp
+
+
+def _check_all(inp):
+    wl = inp.wl
+    d = to_dev(inp)
+    ref = oracle_scores(inp)
+    gs = gpu_scores(inp, d)
+    idx_p, _ = gpu_fused(inp, d, dbg=False)
+    idx_f, dbg = gpu_fused(inp, d, dbg=True)
+    idx_t = csa.index_topk(gs, wl.top_k)
+    assert_status_ok()
+    g = gs.cpu().numpy()
+    check_scores(g, ref)
+    assert np.array_equal(dbg.cpu().numpy(), g)
+    gi = idx_p.cpu().numpy()
+    assert np.array_equal(idx_f.cpu().numpy(), gi)
+    assert np.array_equal(idx_t.cpu().numpy(), gi)
+    check_select_exact(g, gi, wl.top_k)
+    check_select_vs_oracle(ref, gi, wl.top_k)
+
+
+@pytest.mark.parametrize("ci", range(len(EDGE)))
+def test_edge_shapes(ci):
+    _check_all(_edge_inputs(EDGE[ci], seed=ci))
+
+
+@pytest.mark.parametrize("segs", ["packed", "scattered"])
+@pytest.mark.parametrize("ci", [0, 3, 4])
+def test_edge_segments(ci, segs):
+    _check_all(_edge_inputs(EDGE[ci], seed=10 + ci, segs=segs))
+
+
+def test_fp32_weights_large_heads():
+    _check_all(_edge_inputs(dict(B=1, S=260, W=65, H=64, D=128, r=4, top_k=12), seed=3, w_dtype="f32"))
+
+
+# --------------------------------------------------------------------------- invariants on the GPU
+def test_zero_weights_give_zero_scores_and_lowest_indices():
+    inp = _edge_inputs(EDGE[0], seed=21)
+    inp.w = torch.zeros_like(inp.w)
+    d = to_dev(inp)
+    wl = inp.wl
+    g = gpu_scores(inp, d).cpu().numpy()
+    vis = O.visibility(wl.B, wl.S, wl.W, wl.compress_rate)
+    assert np.all(g[vis] == 0.0) and np.all(g[~vis] == -np.inf)
+    idx, _ = gpu_fused(inp, d)
+    ref = O.select_topk(np.where(vis, 0.0, -np.inf), wl.top_k)
+    assert np.array_equal(idx.cpu().numpy(), ref)
+
+
+def test_head_permutation_within_tolerance():
+    inp = _edge_inputs(EDGE[0], seed=22)
+    perm = torch.randperm(inp.wl.H, generator=torch.Generator().manual_seed(1))
+    a = gpu_scores(inp).cpu().numpy()
+    inp2 = Inputs(inp.wl, inp.q[:, perm].contiguous(), inp.k, inp.w[:, :, perm].contiguous(), None, None, None)
+    b = gpu_scores(inp2).cpu().numpy()
+    check_scores(b, a.astype(np.float64))
+
+
+def test_row_slice_matches_full_run():
+    inp = _edge_inputs(dict(B=1, S=400, W=100, H=64, D=128, r=4, top_k=10), seed=23)
+    d = to_dev(inp)
+    wl = inp.wl
+    full = csa.index_fused(d["q"], d["k"], d["w"], wl.scale, 4, wl.top_k)
+    s0, s1 = 123, 301
+    q_start = torch.tensor([s0], dtype=torch.int64, device="cuda")
+    part = csa.index_fused(d["q"][:, :, s0:s1].contiguous(), d["k"], d["w"][:, s0:s1].contiguous(), wl.scale,
+                           4, wl.top_k, q_start=q_start)
+    assert torch.equal(part, full[:, s0:s1])
+
+
+def test_repeated_calls_identical():
+    inp = make_inputs(WORKLOADS["prefill_4k"])
+    d = to_dev(inp)
+    a, _ = gpu_fused(inp, d)
+    b, _ = gpu_fused(inp, d)
+    assert torch.equal(a, b)
+
+
+# --------------------------------------------------------------------------- failure detection
+def test_bounded_wait_gives_up_and_reports():
+    assert csa.device_status() == csa.CSA_OK
+    assert csa.selftest_timeout(20000) == csa.CSA_OK  # 20 ms wait on a barrier nothing completes
+    assert csa.device_status() == csa.CSA_ERR_TIMEOUT
+    assert csa.device_status() == csa.CSA_OK  # the word was cleared
+    # the context is still usable
+    test_hand_example_exact(4, 32)
+
+
+def test_invalid_arguments_on_device_tensors():
+    inp = make_inputs(WORKLOADS["tiny"])
+    d = to_dev(inp)
+    p = csa.make_problem(d["q"], d["k"], d["w"], 0.1, 4, 16)
+    out = torch.empty(1, 256, 64, device="cuda")
+    p.scale = -1.0
+    assert csa.index_score_raw(p, d["q"], d["k"], d["w"], None, None, None, out) == csa.CSA_ERR_INVALID_ARG
+    p.scale = 0.1
+    p.H = 8
+    assert csa.index_score_raw(p, d["q"], d["k"], d["w"], None, None, None, out) == csa.CSA_ERR_UNSUPPORTED
