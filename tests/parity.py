@@ -70,7 +70,7 @@ def check_scores(g: np.ndarray, ref: np.ndarray):
     assert np.array_equal(fin, np.isfinite(g)), "mask differs (finite vs -inf)"
     assert np.all(g[~fin] == -np.inf) and np.all(ref[~fin] == -np.inf)
     rowmax = np.max(np.where(fin, np.abs(ref), 0.0), axis=-1, keepdims=True)
-    err = np.abs(np.where(fin, g - ref, 0.0))
+    err = np.abs(np.where(fin, g, 0.0) - np.where(fin, ref, 0.0))
     bad = err > TOL * rowmax
     assert not bad.any(), (f"{int(bad.sum())} scores outside tolerance; worst rel "
                            f"{float((err / np.maximum(rowmax, 1e-300)).max()):.3e}")
