@@ -8,7 +8,7 @@
 #include <cstring>
 #include <mutex>
 
-#include "../../include/csa_index.h"
+#include "csa_index.h"
 #include "csa_internal.h"
 
 namespace csa {

@@ -25,7 +25,6 @@ size_t index_kernel_smem(const KernelChoice& kc, int w_pad);
 // Standalone per-row selection over [rows, W] fp32 scores.
 cudaError_t launch_topk(const float* scores, int32_t* idx, long long rows, int W, int K,
                         cudaStream_t stream);
-size_t topk_smem(int W);
 int topk_threads(int W);
 
 // Kernel that waits on a barrier nothing completes, bounded by `ns`.

@@ -18,13 +18,13 @@
 // Warp roles (block = 4 control warps + EW epilogue warps):
 //   warp 0  TMA producer: q block per item, k tiles into a ring of stages
 //   warp 1  TMEM owner and UMMA issuer (one elected thread)
-//   warp 2  scheduler: per item computes the visible tile range, per-row
-//           thresholds / segment ids / visible counts and stages the
-//           weights into a ring of item slots
-//   warp 3  idle
+//   warps 2, 3  schedulers (alternate items): per item compute the visible
+//           tile range, per-row thresholds / segment ids / visible counts and
+//           stage the weights into a ring of item slots
 //   warps 4..4+EW-1  epilogue (warp w reads TMEM lanes 32*(w%4) ..)
-// FUSED: scores stay in shared memory ([R][W] fp32) and the epilogue warps
-// then run the per-row selection, two warps per row.
+// FUSED: scores stay in shared memory ([R][W] fp32) together with per-row
+// visible counts and value ranges, and the epilogue warps then run the
+// per-row selection, two warps per row.
 //
 // Tiles wholly past the rows' future-mask bound, or (with segment ids)
 // outside the range of entries sharing a segment with the item's rows, are
@@ -37,7 +37,6 @@
 namespace csa {
 
 constexpr int kTileT = 128;  // compressed entries per tile (UMMA M)
-constexpr int kSlots = 4;    // item ring depth
 
 struct KParams {
   int B, S, W, r, K;
@@ -62,7 +61,15 @@ struct ItemDesc {
   int trivial;     // fused: every row keeps all its visible entries, no scores needed
   int thr[R];      // rows' visible bound min(W, (pos+1)/r); 0 for rows past S
   int seg[R];
-  int nvis[R];
+  int nvis[R];     // visible entries of the row inside [c_lo, c_hi) tiles
+  int tfirst[R];   // first visible entry of the row
+  int contig[R];   // the row's visible entries are tfirst .. tfirst + nvis - 1
+};
+
+// Selection scratch of one row team of the fused kernel.
+struct FusedRowScratch {
+  SelectScratch sc;
+  BinScratch<512, 256, 128> bs;  // rows of up to 4096 entries
 };
 
 constexpr uint32_t pow2_cols(uint32_t n) {
@@ -83,12 +90,14 @@ struct Cfg {
   static_assert(D % 32 == 0, "head dim must be a multiple of 32");
   static constexpr int KSTAGES = (R == 1) ? 5 : 2;
   static constexpr int QBUF = FUSED ? 1 : 2;
-  static constexpr int EW = (R >= 2) ? 8 : 4;  // epilogue warps
+  static constexpr int SLOTS = 4;                  // item ring depth
+  static constexpr int EW = (R >= 2) ? 8 : 4;      // epilogue warps
   static constexpr int RW = (R >= 2) ? R / 2 : 1;  // rows per epilogue warp
   static_assert(R == 1 || R % 2 == 0, "R must be 1 or even");
+  static_assert(!FUSED || R == 4, "the fused selection runs two warps on each of four rows");
   static constexpr int NTHREADS = 128 + EW * 32;
-  static constexpr uint32_t QCHUNK = N * ROWB;        // bytes of one K-chunk of the q block
-  static constexpr uint32_t KCHUNK = kTileT * ROWB;   // bytes of one K-chunk of a k tile
+  static constexpr uint32_t QCHUNK = N * ROWB;       // bytes of one K-chunk of the q block
+  static constexpr uint32_t KCHUNK = kTileT * ROWB;  // bytes of one K-chunk of a k tile
   static constexpr uint32_t QBYTES = QCHUNK * NKC;
   static constexpr uint32_t KBYTES = KCHUNK * NKC;
   static constexpr uint32_t TMEM_COLS = pow2_cols(2 * N);
@@ -97,15 +106,16 @@ struct Cfg {
   static constexpr uint32_t OFF_Q = 0;
   static constexpr uint32_t OFF_K = (OFF_Q + QBUF * QBYTES + 1023) & ~1023u;
   static constexpr uint32_t OFF_W = (OFF_K + KSTAGES * KBYTES + 1023) & ~1023u;
-  static constexpr uint32_t OFF_DESC = OFF_W + kSlots * R * H * 4;
-  static constexpr uint32_t OFF_BAR = (OFF_DESC + kSlots * sizeof(ItemDesc<R>) + 15) & ~15u;
-  // barriers: item_full[S], item_empty[S], q_full[QB], q_empty[QB], k_full[KS], k_empty[KS],
+  static constexpr uint32_t OFF_DESC = OFF_W + SLOTS * R * H * 4;
+  static constexpr uint32_t OFF_BAR = (OFF_DESC + SLOTS * sizeof(ItemDesc<R>) + 15) & ~15u;
+  // barriers: item_full[SLOTS], item_empty[SLOTS], q_full[QB], q_empty[QB], k_full[KS], k_empty[KS],
   //           acc_full[2], acc_empty[2], drain
-  static constexpr int NBAR = 2 * kSlots + 2 * QBUF + 2 * KSTAGES + 4 + 1;
+  static constexpr int NBAR = 2 * SLOTS + 2 * QBUF + 2 * KSTAGES + 4 + 1;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;  // tmem base, abort flag
-  static constexpr uint32_t OFF_SCR = (OFF_MISC + 16 + 15) & ~15u;
+  static constexpr uint32_t OFF_STATS = (OFF_MISC + 16 + 15) & ~15u;  // RowStats[R]
+  static constexpr uint32_t OFF_SCR = (OFF_STATS + R * sizeof(RowStats) + 15) & ~15u;
   static constexpr uint32_t NSCR = FUSED ? R : 0;
-  static constexpr uint32_t OFF_SROW = (OFF_SCR + NSCR * sizeof(SelectScratch) + 127) & ~127u;
+  static constexpr uint32_t OFF_SROW = (OFF_SCR + NSCR * sizeof(FusedRowScratch) + 127) & ~127u;
   // dynamic shared memory for a given fused row pitch (+1 KB alignment slack)
   static constexpr uint32_t smem_bytes(int w_pad) {
     return OFF_SROW + (FUSED ? (uint32_t)R * (uint32_t)w_pad * 4u : 0u) + 1024u;
@@ -115,6 +125,9 @@ struct Cfg {
 template <class C>
 struct Smem {
   uint8_t* base;
+  static constexpr int B0 = 2 * C::SLOTS;         // first q barrier
+  static constexpr int B1 = B0 + 2 * C::QBUF;     // first k barrier
+  static constexpr int B2 = B1 + 2 * C::KSTAGES;  // first accumulator barrier
   __device__ uint8_t* q(int i) const { return base + C::OFF_Q + i * C::QBYTES; }
   __device__ uint8_t* k(int i) const { return base + C::OFF_K + i * C::KBYTES; }
   __device__ float* w(int slot) const { return reinterpret_cast<float*>(base + C::OFF_W) + slot * C::R * C::H; }
@@ -123,20 +136,21 @@ struct Smem {
   }
   __device__ uint64_t* bar(int i) const { return reinterpret_cast<uint64_t*>(base + C::OFF_BAR) + i; }
   __device__ uint64_t* item_full(int s) const { return bar(s); }
-  __device__ uint64_t* item_empty(int s) const { return bar(kSlots + s); }
-  __device__ uint64_t* q_full(int i) const { return bar(2 * kSlots + i); }
-  __device__ uint64_t* q_empty(int i) const { return bar(2 * kSlots + C::QBUF + i); }
-  __device__ uint64_t* k_full(int i) const { return bar(2 * kSlots + 2 * C::QBUF + i); }
-  __device__ uint64_t* k_empty(int i) const { return bar(2 * kSlots + 2 * C::QBUF + C::KSTAGES + i); }
-  __device__ uint64_t* acc_full(int i) const { return bar(2 * kSlots + 2 * C::QBUF + 2 * C::KSTAGES + i); }
-  __device__ uint64_t* acc_empty(int i) const { return bar(2 * kSlots + 2 * C::QBUF + 2 * C::KSTAGES + 2 + i); }
-  __device__ uint64_t* drain() const { return bar(2 * kSlots + 2 * C::QBUF + 2 * C::KSTAGES + 4); }
+  __device__ uint64_t* item_empty(int s) const { return bar(C::SLOTS + s); }
+  __device__ uint64_t* q_full(int i) const { return bar(B0 + i); }
+  __device__ uint64_t* q_empty(int i) const { return bar(B0 + C::QBUF + i); }
+  __device__ uint64_t* k_full(int i) const { return bar(B1 + i); }
+  __device__ uint64_t* k_empty(int i) const { return bar(B1 + C::KSTAGES + i); }
+  __device__ uint64_t* acc_full(int i) const { return bar(B2 + i); }
+  __device__ uint64_t* acc_empty(int i) const { return bar(B2 + 2 + i); }
+  __device__ uint64_t* drain() const { return bar(B2 + 4); }
   __device__ uint32_t* tmem_slot() const { return reinterpret_cast<uint32_t*>(base + C::OFF_MISC); }
   __device__ volatile uint32_t* abort_flag() const {
     return reinterpret_cast<volatile uint32_t*>(base + C::OFF_MISC + 4);
   }
-  __device__ SelectScratch* scratch(int j) const {
-    return reinterpret_cast<SelectScratch*>(base + C::OFF_SCR) + j;
+  __device__ RowStats* stats(int j) const { return reinterpret_cast<RowStats*>(base + C::OFF_STATS) + j; }
+  __device__ FusedRowScratch* scratch(int j) const {
+    return reinterpret_cast<FusedRowScratch*>(base + C::OFF_SCR) + j;
   }
   __device__ float* srow(int j, int w_pad) const {
     return reinterpret_cast<float*>(base + C::OFF_SROW) + (size_t)j * w_pad;
@@ -153,20 +167,22 @@ __device__ __forceinline__ void item_coords(const KParams& p, int item, int& b, 
   rb = p.n_rb - 1 - rest / p.B;
 }
 
+// Scheduler warp `sw` (0 or 1) prepares the items with it % 2 == sw.
 template <class C>
-__device__ void run_scheduler(const KParams& p, const Smem<C>& sm, const WaitCtl& ctl) {
+__device__ void run_scheduler(const KParams& p, const Smem<C>& sm, const WaitCtl& ctl, int sw) {
   constexpr int R = C::R, H = C::H;
   const uint32_t lane = lane_id();
   const bool segs = p.q_seg != nullptr;
   int it = 0;
   for (int item = blockIdx.x; item < p.n_items; item += gridDim.x, ++it) {
-    const int slot = it % kSlots;
-    mbar_wait(sm.item_empty(slot), ((it / kSlots) & 1) ^ 1, ctl);
+    if ((it & 1) != sw) continue;
+    const int slot = it % C::SLOTS;
+    mbar_wait(sm.item_empty(slot), ((it / C::SLOTS) & 1) ^ 1, ctl);
     int b, rb, c;
     item_coords(p, item, b, rb, c);
     const int s0 = rb * R;
     const long long qs0 = p.q_start ? (long long)p.q_start[b] : 0ll;
-    int thr[R], seg[R], nvis[R];
+    int thr[R], seg[R], nvis[R], tfirst[R], contig[R];
     int thr_max = 0;
 #pragma unroll
     for (int j = 0; j < R; ++j) {
@@ -185,33 +201,74 @@ __device__ void run_scheduler(const KParams& p, const Smem<C>& sm, const WaitCtl
     int t_lo = c_lo, t_hi = c_lo;
     if (!segs) {
 #pragma unroll
-      for (int j = 0; j < R; ++j) nvis[j] = max(0, min(thr[j], c_hi * kTileT) - c_lo * kTileT);
+      for (int j = 0; j < R; ++j) {
+        nvis[j] = max(0, min(thr[j], c_hi * kTileT) - c_lo * kTileT);
+        tfirst[j] = c_lo * kTileT;
+        contig[j] = 1;
+      }
       t_hi = max(c_lo, min(c_hi, (thr_max + kTileT - 1) / kTileT));
     } else {
-      int cnt[R];
+      int cnt[R], tmn[R], tmx[R];
 #pragma unroll
-      for (int j = 0; j < R; ++j) cnt[j] = 0;
-      int tmin = 0x7FFFFFFF, tmax = -1;
+      for (int j = 0; j < R; ++j) {
+        cnt[j] = 0;
+        tmn[j] = 0x7FFFFFFF;
+        tmx[j] = -1;
+      }
+      const int e_lo = c_lo * kTileT;
       const int e_hi = min(c_hi * kTileT, thr_max);
       const int32_t* kv = p.kv_seg + (size_t)b * p.W;
-      for (int t = c_lo * kTileT + (int)lane; t < e_hi; t += 32) {
-        const int ks = kv[t];
-        bool any = false;
+      const bool vec = ((reinterpret_cast<uintptr_t>(kv) & 15u) == 0) && (e_lo % 4 == 0);
+      auto visit = [&](int t, int ks) {
 #pragma unroll
         for (int j = 0; j < R; ++j) {
           const bool m = (t < thr[j]) && (ks == seg[j]);
           cnt[j] += m;
-          any |= m;
+          if (m) {
+            tmn[j] = min(tmn[j], t);
+            tmx[j] = max(tmx[j], t);
+          }
         }
-        if (any) {
-          tmin = min(tmin, t);
-          tmax = max(tmax, t);
+      };
+      if (vec) {
+        // four 16-byte loads in flight per lane per round (512 entries per warp)
+        for (int t0 = e_lo + 4 * (int)lane; t0 < e_hi; t0 += 512) {
+          int4 v4[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int t = t0 + 128 * u;
+            v4[u] = (t + 3 < e_hi) ? *reinterpret_cast<const int4*>(kv + t) : make_int4(0, 0, 0, 0);
+          }
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int t = t0 + 128 * u;
+            if (t + 3 < e_hi) {
+              visit(t, v4[u].x);
+              visit(t + 1, v4[u].y);
+              visit(t + 2, v4[u].z);
+              visit(t + 3, v4[u].w);
+            } else {
+              for (int x = t; x < e_hi; ++x) visit(x, kv[x]);
+            }
+          }
+        }
+      } else {
+        for (int t = e_lo + (int)lane; t < e_hi; t += 32) visit(t, kv[t]);
+      }
+      int tmin = 0x7FFFFFFF, tmax = -1;
+#pragma unroll
+      for (int j = 0; j < R; ++j) {
+        nvis[j] = (int)__reduce_add_sync(0xFFFFFFFFu, (unsigned)cnt[j]);
+        tfirst[j] = __reduce_min_sync(0xFFFFFFFFu, tmn[j]);
+        const int last = __reduce_max_sync(0xFFFFFFFFu, tmx[j]);
+        contig[j] = (nvis[j] == 0) || (last - tfirst[j] + 1 == nvis[j]);
+        if (nvis[j] > 0) {
+          tmin = min(tmin, tfirst[j]);
+          tmax = max(tmax, last);
+        } else {
+          tfirst[j] = 0;
         }
       }
-#pragma unroll
-      for (int j = 0; j < R; ++j) nvis[j] = (int)__reduce_add_sync(0xFFFFFFFFu, (unsigned)cnt[j]);
-      tmin = __reduce_min_sync(0xFFFFFFFFu, tmin);
-      tmax = __reduce_max_sync(0xFFFFFFFFu, tmax);
       if (tmax >= 0) {
         t_lo = tmin / kTileT;
         t_hi = tmax / kTileT + 1;
@@ -251,6 +308,8 @@ __device__ void run_scheduler(const KParams& p, const Smem<C>& sm, const WaitCtl
         d->thr[j] = thr[j];
         d->seg[j] = seg[j];
         d->nvis[j] = nvis[j];
+        d->tfirst[j] = tfirst[j];
+        d->contig[j] = contig[j];
       }
     }
     __syncwarp();
@@ -264,8 +323,8 @@ __device__ void run_producer(const KParams& p, const Smem<C>& sm, const WaitCtl&
   uint32_t kcount = 0, qcount = 0;
   int it = 0;
   for (int item = blockIdx.x; item < p.n_items; item += gridDim.x, ++it) {
-    const int slot = it % kSlots;
-    const bool ok_item = mbar_wait(sm.item_full(slot), (it / kSlots) & 1, ctl);
+    const int slot = it % C::SLOTS;
+    const bool ok_item = mbar_wait(sm.item_full(slot), (it / C::SLOTS) & 1, ctl);
     const ItemDesc<C::R>* d = sm.desc(slot);
     const int b = d->b, s0 = d->s0, t_lo = d->t_lo, t_hi = d->t_hi;
     mbar_arrive(sm.item_empty(slot));
@@ -290,9 +349,8 @@ __device__ void run_producer(const KParams& p, const Smem<C>& sm, const WaitCtl&
     }
   }
   // make sure no copy is still landing in shared memory when the CTA exits
-  WaitCtl drain_ctl{ctl.abort_flag, ctl.limit_ns};
   volatile uint32_t dummy = 0;
-  drain_ctl.abort_flag = &dummy;
+  const WaitCtl drain_ctl{&dummy, ctl.limit_ns};
   for (uint32_t i = 0; i < C::KSTAGES && i < kcount; ++i) {
     const uint32_t last = kcount - 1 - i;  // most recent use of stage last % KSTAGES
     mbar_wait(sm.k_full(last % C::KSTAGES), (last / C::KSTAGES) & 1, drain_ctl);
@@ -308,8 +366,8 @@ __device__ void run_mma(const KParams& p, const Smem<C>& sm, const WaitCtl& ctl,
   uint32_t kcount = 0, qcount = 0, acount = 0;
   int it = 0;
   for (int item = blockIdx.x; item < p.n_items; item += gridDim.x, ++it) {
-    const int slot = it % kSlots;
-    const bool ok_item = mbar_wait(sm.item_full(slot), (it / kSlots) & 1, ctl);
+    const int slot = it % C::SLOTS;
+    const bool ok_item = mbar_wait(sm.item_full(slot), (it / C::SLOTS) & 1, ctl);
     const ItemDesc<C::R>* d = sm.desc(slot);
     const int t_lo = d->t_lo, t_hi = d->t_hi;
     mbar_arrive(sm.item_empty(slot));
@@ -348,7 +406,7 @@ __device__ void run_mma(const KParams& p, const Smem<C>& sm, const WaitCtl& ctl,
   // every MMA issued above has completed once this barrier fires
   umma_commit(sm.drain());
   volatile uint32_t dummy = 0;
-  WaitCtl drain_ctl{&dummy, ctl.limit_ns};
+  const WaitCtl drain_ctl{&dummy, ctl.limit_ns};
   mbar_wait(sm.drain(), 0, drain_ctl);
 }
 
@@ -359,23 +417,24 @@ __device__ __forceinline__ void epilogue_accumulate(uint32_t t_row, const float*
   constexpr int H = C::H, RW = C::RW;
 #pragma unroll
   for (int jj = 0; jj < RW; ++jj) acc[jj] = 0.f;
-  if constexpr (H % 32 == 0) {
+  if constexpr (H == 64) {
+    // one 64-column TMEM load per row (all heads of the row); four
+    // independent packed-FMA chains
 #pragma unroll
     for (int jj = 0; jj < RW; ++jj) {
       const int j = hf * RW + jj;
-      float2 a2 = make_float2(0.f, 0.f);
+      float v[64];
+      tmem_ld64(t_row + (uint32_t)(j * H), v);
+      const float2* w2 = reinterpret_cast<const float2*>(ws + j * H);
+      float2 a[4];
 #pragma unroll
-      for (int hc = 0; hc < H / 32; ++hc) {
-        float v[32];
-        tmem_ld32(t_row + (uint32_t)(j * H + hc * 32), v);
-        const float2* w2 = reinterpret_cast<const float2*>(ws + j * H + hc * 32);
+      for (int q = 0; q < 4; ++q) a[q] = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float2 r2 = make_float2(fmaxf(v[2 * i], 0.f), fmaxf(v[2 * i + 1], 0.f));
-          a2 = ffma2(w2[i], r2, a2);
-        }
+      for (int i = 0; i < H / 2; ++i) {
+        const float2 r2 = make_float2(fmaxf(v[2 * i], 0.f), fmaxf(v[2 * i + 1], 0.f));
+        a[i & 3] = ffma2(w2[i], r2, a[i & 3]);
       }
-      acc[jj] = a2.x + a2.y;
+      acc[jj] = ((a[0].x + a[0].y) + (a[1].x + a[1].y)) + ((a[2].x + a[2].y) + (a[3].x + a[3].y));
     }
   } else {
     static_assert((C::RW * H) % 8 == 0, "small-head path loads 8 columns at a time");
@@ -393,6 +452,31 @@ __device__ __forceinline__ void epilogue_accumulate(uint32_t t_row, const float*
   }
 }
 
+// Write the selection of a row that keeps all its visible entries.
+template <int NT>
+__device__ void write_visible_set(int32_t* out, int K, int nvis, int tfirst, int contig, int thr, int seg,
+                                  const int32_t* kv, SelectScratch* sc, const Team<NT>& team) {
+  if (contig) {  // visible entries are tfirst .. tfirst + nvis - 1
+    if ((K & 3) == 0 && (reinterpret_cast<uintptr_t>(out) & 15u) == 0) {
+      int4* o4 = reinterpret_cast<int4*>(out);
+      for (int i = (int)team.tid; i < K / 4; i += NT) {
+        const int i0 = 4 * i;
+        int4 v;
+        v.x = (i0 + 0 < nvis) ? tfirst + i0 + 0 : -1;
+        v.y = (i0 + 1 < nvis) ? tfirst + i0 + 1 : -1;
+        v.z = (i0 + 2 < nvis) ? tfirst + i0 + 2 : -1;
+        v.w = (i0 + 3 < nvis) ? tfirst + i0 + 3 : -1;
+        o4[i] = v;
+      }
+    } else {
+      for (int i = (int)team.tid; i < K; i += NT) out[i] = (i < nvis) ? tfirst + i : -1;
+    }
+  } else {
+    team_write_ordered<NT>(0, thr, 0u, (uint32_t)K, out, sc, team,
+                           [&](int tt) -> int { return (kv[tt] == seg) ? 1 : 0; });
+  }
+}
+
 template <class C>
 __device__ void run_epilogue(const KParams& p, const Smem<C>& sm, const WaitCtl& ctl, uint32_t tmem_base,
                              int e /* epilogue warp 0..EW-1 */) {
@@ -405,16 +489,21 @@ __device__ void run_epilogue(const KParams& p, const Smem<C>& sm, const WaitCtl&
   uint32_t acount = 0;
   int it = 0;
   for (int item = blockIdx.x; item < p.n_items; item += gridDim.x, ++it) {
-    const int slot = it % kSlots;
-    mbar_wait(sm.item_full(slot), (it / kSlots) & 1, ctl);
+    const int slot = it % C::SLOTS;
+    mbar_wait(sm.item_full(slot), (it / C::SLOTS) & 1, ctl);
     const ItemDesc<R>* d = sm.desc(slot);
     const int b = d->b, s0 = d->s0, t_lo = d->t_lo, t_hi = d->t_hi, c_lo = d->c_lo, c_hi = d->c_hi;
     const int trivial = d->trivial;
     int thr[RW], seg[RW];
+    float smin[RW], smax[RW];
+    uint32_t scnt[RW];
 #pragma unroll
     for (int jj = 0; jj < RW; ++jj) {
       thr[jj] = d->thr[hf * RW + jj];
       seg[jj] = d->seg[hf * RW + jj];
+      smin[jj] = INFINITY;
+      smax[jj] = -INFINITY;
+      scnt[jj] = 0u;
     }
     const float* ws = sm.w(slot);
     const bool write_all = !C::FUSED || p.scores != nullptr;
@@ -446,34 +535,53 @@ __device__ void run_epilogue(const KParams& p, const Smem<C>& sm, const WaitCtl&
         const float val = vis ? p.scale * acc[jj] : -INFINITY;
         if constexpr (C::FUSED) {
           if (t < p.w_pad) sm.srow(j, p.w_pad)[t] = val;
+          if (vis) {
+            smin[jj] = fminf(smin[jj], val);
+            smax[jj] = fmaxf(smax[jj], val);
+            scnt[jj] += 1u;
+          }
         }
         if (p.scores != nullptr && s < p.S && t < p.W) p.scores[((size_t)b * p.S + s) * p.W + t] = val;
       }
     }
     if constexpr (C::FUSED) {
-      named_bar_sync(1, C::EW * 32);  // the item's scores are in shared memory
-      const int j = e / 2;            // two warps per row
-      const int s = s0 + j;
-      Team<64> team{(uint32_t)(2 + j), (uint32_t)((e & 1) * 32) + lane};
-      if (j < R && s < p.S) {
-        int32_t* out = p.idx + ((size_t)b * p.S + s) * p.K;
-        const int thr_j = d->thr[j];
-        const int seg_j = d->seg[j];
-        if (trivial) {
-          if (!segs) {
-            for (int i = (int)team.tid; i < p.K; i += 64) out[i] = (i < thr_j) ? i : -1;
-          } else {
-            const int32_t* kv = p.kv_seg + (size_t)b * p.W;
-            team_write_ordered<64>(0, thr_j, 0u, (uint32_t)p.K, out, sm.scratch(j), team,
-                                   [&](int tt) -> int { return (kv[tt] == seg_j) ? 1 : 0; });
+      if (!trivial) {  // fold this warp's row statistics into the shared per-row ones
+#pragma unroll
+        for (int jj = 0; jj < RW; ++jj) {
+          const uint32_t cnt = __reduce_add_sync(0xFFFFFFFFu, scnt[jj]);
+          const uint32_t kmin = __reduce_min_sync(0xFFFFFFFFu, score_key(smin[jj]));
+          const uint32_t kmax = __reduce_max_sync(0xFFFFFFFFu, score_key(smax[jj]));
+          if (lane == 0 && cnt > 0u) {
+            RowStats* st = sm.stats(hf * RW + jj);
+            atomicAdd(&st->nvis, cnt);
+            atomicMin(&st->min_key, kmin);
+            atomicMax(&st->max_key, kmax);
           }
-        } else {
-          const int e_lo = t_lo * kTileT;
-          const int e_hi = min(t_hi * kTileT, p.W);
-          team_topk_row<64>(sm.srow(j, p.w_pad), e_lo, e_hi, (uint32_t)p.K, out, sm.scratch(j), team);
         }
       }
-      named_bar_sync(1, C::EW * 32);  // shared score rows may be overwritten
+      named_bar_sync(1, C::EW * 32);  // the item's scores and row statistics are in shared memory
+      const int j = e / 2;            // two warps per row
+      const int s = s0 + j;
+      const Team<64> team{(uint32_t)(2 + j), (uint32_t)((e & 1) * 32) + lane};
+      if (s < p.S) {
+        int32_t* out = p.idx + ((size_t)b * p.S + s) * p.K;
+        FusedRowScratch* fs = sm.scratch(j);
+        if (trivial) {
+          write_visible_set<64>(out, p.K, d->nvis[j], d->tfirst[j], d->contig[j], d->thr[j], d->seg[j],
+                                p.kv_seg + (size_t)b * p.W, &fs->sc, team);
+        } else {
+          const RowStats st = *sm.stats(j);
+          team_topk_row(sm.srow(j, p.w_pad), t_lo * kTileT, (t_hi - t_lo) * kTileT, (uint32_t)p.K, st, out,
+                        &fs->bs, &fs->sc, team);
+          if (team.tid == 0) {
+            RowStats* w = sm.stats(j);
+            w->nvis = 0u;
+            w->min_key = 0xFFFFFFFFu;
+            w->max_key = 0u;
+          }
+        }
+      }
+      named_bar_sync(1, C::EW * 32);  // shared score rows and statistics may be overwritten
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(sm.item_empty(slot));
@@ -491,7 +599,7 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
   const uint32_t lane = lane_id();
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kSlots; ++s) {
+    for (int s = 0; s < C::SLOTS; ++s) {
       mbar_init(sm.item_full(s), 1);
       mbar_init(sm.item_empty(s), 2 + C::EW);
     }
@@ -509,6 +617,11 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
     }
     mbar_init(sm.drain(), 1);
     *sm.abort_flag() = 0u;
+    for (int j = 0; j < C::R; ++j) {
+      sm.stats(j)->nvis = 0u;
+      sm.stats(j)->min_key = 0xFFFFFFFFu;
+      sm.stats(j)->max_key = 0u;
+    }
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
@@ -529,11 +642,12 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
     if (lane == 0) run_producer<C>(p, sm, ctl, &tmap_q, &tmap_k);
   } else if (warp == 1) {
     if (lane == 0) run_mma<C>(p, sm, ctl, tmem_base);
-  } else if (warp == 2) {
-    run_scheduler<C>(p, sm, ctl);
-  } else if (warp >= 4) {
+  } else if (warp == 2 || warp == 3) {
+    run_scheduler<C>(p, sm, ctl, warp - 2);
+  } else {
     run_epilogue<C>(p, sm, ctl, tmem_base, warp - 4);
   }
+  __syncwarp();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();

@@ -7,12 +7,22 @@
 // largest, equal scores going to the lower entry index and comparing by value
 // (-0.0 == +0.0); write the kept indices ascending and pad with -1.
 //
-// Method: scores map to order-preserving 32-bit keys (0 = invisible).  A
-// most-significant-digit-first radix search (four 8-bit digits) finds the
-// K-th largest key T and how many keys equal to T are kept (the lowest
-// indices first).  One ordered compaction pass then writes, per row, every
-// index whose key is above T plus the first `take_eq` indices whose key
-// equals T, in ascending order.
+// Method (team_topk_row): scores map to order-preserving 32-bit keys (0 =
+// invisible).  With the row's visible count and value range known,
+//   1. a histogram of NB bins spaced linearly between the row's smallest and
+//      largest visible score (a monotone map, so bins are ordered value
+//      intervals and a row's scores spread over many bins);
+//   2. the bin b* holding the K-th largest score (team-wide suffix scan);
+//   3. one pass per warp over a contiguous segment: a ballot bitmap of the
+//      entries in bins above b* (kept for sure), per-segment counts, and the
+//      members of b* gathered with their entry numbers;
+//   4. an exact rank of the gathered members by (value desc, index asc);
+//   5. an ordered write from the bitmap (popcounts only).
+// Rows that keep all their visible entries, rows of equal scores, rows whose
+// value range overflows fp32 and rows whose b* holds more than CAP members
+// take the general path: a most-significant-digit-first radix search over
+// the keys (four 8-bit digits) for the K-th largest key T and the number of
+// keys equal to T that are kept, then an ordered compaction.
 #pragma once
 
 #include "csa_ptx.cuh"
@@ -27,6 +37,12 @@ __device__ __forceinline__ uint32_t score_key(float f) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+// Inverse of score_key for a visible key.
+__device__ __forceinline__ float key_score(uint32_t k) {
+  const uint32_t u = (k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k;
+  return __uint_as_float(u);
+}
+
 struct SelectScratch {
   uint32_t hist[256];
   uint32_t warp_a[32];
@@ -34,10 +50,33 @@ struct SelectScratch {
   uint32_t bcast[4];
 };
 
+// Scratch of the binned search: NB histogram bins, up to CAP gathered
+// (key, entry) pairs of the threshold bin, and a keep-bitmap of up to MAXW
+// words (word 4*c+u holds bit `lane` for entry c*128 + 4*lane + u).
+template <int NB, int CAP, int MAXW>
+struct BinScratch {
+  uint32_t hist[NB];
+  uint32_t cand[CAP];
+  uint32_t cand_t[CAP];
+  uint32_t seg_gt[32];   // per warp segment: entries in bins above the threshold bin
+  uint32_t seg_sel[32];  // per warp segment: kept entries of the threshold bin
+  uint32_t warp_sum[32];
+  uint32_t bcast[4];
+  uint32_t keep[MAXW];
+};
+
+// Visible count and value range of one row.
+struct RowStats {
+  uint32_t nvis;
+  uint32_t min_key;  // score_key of the smallest visible score
+  uint32_t max_key;  // score_key of the largest visible score
+};
+
 // A team: NT threads (a multiple of 32) synchronised by named barrier `bar_id`.
 template <int NT>
 struct Team {
   static_assert(NT % 32 == 0, "team size must be whole warps");
+  static constexpr int kThreads = NT;
   uint32_t bar_id;
   uint32_t tid;  // 0 .. NT-1
   __device__ __forceinline__ void sync() const {
@@ -98,19 +137,20 @@ __device__ SelectResult team_select_threshold(const float* row, int t_begin, int
       }
       __syncwarp();
       if (here) {
-        uint32_t acc = excl;
-        int d = 0;
+        uint32_t acc = excl, d = 0, cd = 0;
+        bool found = false;
 #pragma unroll
         for (int j = 7; j >= 0; --j) {
-          if (acc + c[j] >= r) {
-            d = j;
-            break;
+          if (!found && acc + c[j] >= r) {
+            found = true;
+            d = (uint32_t)j;
+            cd = c[j];
           }
-          acc += c[j];
+          if (!found) acc += c[j];
         }
-        sc->bcast[0] = lane * 8 + (uint32_t)d;  // digit
-        sc->bcast[1] = acc;                      // keys strictly above the digit's bin
-        sc->bcast[2] = c[d];                     // keys inside the digit's bin
+        sc->bcast[0] = lane * 8 + d;  // digit
+        sc->bcast[1] = acc;           // keys strictly above the digit's bin
+        sc->bcast[2] = cd;            // keys inside the digit's bin
       }
     }
     team.sync();
@@ -202,18 +242,207 @@ __device__ void team_write_ordered(int t_begin, int t_end, uint32_t take_eq, uin
   team.sync();  // scratch reuse by the caller
 }
 
-// Full selection of one row held in shared memory.
+// Cold paths kept out of line so the hot selection stays small in the
+// instruction cache: the radix search and the general ordered write.
 template <int NT>
-__device__ void team_topk_row(const float* row, int t_begin, int t_end, uint32_t K, int32_t* out,
-                              SelectScratch* sc, const Team<NT>& team) {
-  const SelectResult r = team_select_threshold<NT>(row, t_begin, t_end, K, sc, team);
-  const uint32_t T = r.T;
-  team_write_ordered<NT>(t_begin, t_end, r.take_eq, K, out, sc, team, [&](int t) -> int {
+__device__ __noinline__ void select_general(const float* row, int t0, int n, uint32_t K, uint32_t T,
+                                            uint32_t take_eq, bool search, int32_t* out, SelectScratch* sc,
+                                            uint32_t bar_id, uint32_t tid) {
+  const Team<NT> team{bar_id, tid};
+  if (search) {
+    const SelectResult r = team_select_threshold<NT>(row, t0, t0 + n, K, sc, team);
+    T = r.T;
+    take_eq = r.take_eq;
+  }
+  team_write_ordered<NT>(t0, t0 + n, take_eq, K, out, sc, team, [&](int t) -> int {
     const uint32_t key = score_key(row[t]);
     if (key == 0u) return 0;
     if (key > T) return 1;
     return (key == T) ? 2 : 0;
   });
+}
+
+// Selection of one row whose scores live in shared memory at row[t0, t0+n):
+// t0 and n multiples of 128, row 16-byte aligned, entries past the row's end
+// hold -inf; the indices written are absolute entry numbers.  `st` holds the
+// row's visible count and value range.  The bin of x is
+// round(clamp(x*scale + bias, 0, NB-1)) read from the mantissa of that value
+// plus 2^23: a monotone map of x, identical in every pass.
+template <int NT, int NB, int CAP, int MAXW>
+__device__ void team_topk_row(float* row, int t0, int n, uint32_t K, const RowStats& st, int32_t* out,
+                              BinScratch<NB, CAP, MAXW>* bs, SelectScratch* sc, const Team<NT>& team) {
+  constexpr int NW = NT / 32;
+  constexpr int PER = NB / NT;  // bins per thread in the scan
+  static_assert(NB % NT == 0 && PER >= 1, "bins must be a multiple of the team size");
+  const uint32_t lane = team.tid & 31u, warp = team.warp();
+  const float lo = key_score(st.min_key), hi = key_score(st.max_key);
+  const float span = hi - lo;
+  const float scale = (float)(NB - 1) / span;
+  const int chunks = n >> 7;
+  if (st.nvis <= K) {
+    select_general<NT>(row, t0, n, K, 0u, 0u, false, out, sc, team.bar_id, team.tid);
+    return;
+  }
+  if (!(hi > lo)) {
+    select_general<NT>(row, t0, n, K, st.min_key, K, false, out, sc, team.bar_id, team.tid);
+    return;
+  }
+  const float bias = -lo * scale;
+  // |bias| < 2^21 keeps the rounding of x*scale + bias within a quarter bin,
+  // so the bin map below stays monotone and in range
+  if (!(span < INFINITY) || !(scale < INFINITY) || !(fabsf(bias) < 2097152.0f) || chunks * 4 > MAXW) {
+    select_general<NT>(row, t0, n, K, 0u, 0u, true, out, sc, team.bar_id, team.tid);
+    return;
+  }
+  const float nb1 = (float)(NB - 1);
+  auto bin_of = [&](float x) -> uint32_t {  // in [0, NB-1] for any finite x
+    return __float_as_uint(fmaxf(fminf(fmaf(x, scale, bias), nb1), 0.0f) + 8388608.0f) - 0x4B000000u;
+  };
+  const float4* row4 = reinterpret_cast<const float4*>(row + t0);
+  const int n4 = n >> 2;
+  const float4 ninf4 = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+#pragma unroll
+  for (int j = 0; j < PER; ++j) bs->hist[team.tid * PER + j] = 0u;
+  if (team.tid < 32) {
+    bs->seg_gt[team.tid] = 0u;
+    bs->seg_sel[team.tid] = 0u;
+  }
+  team.sync();
+  // 1. histogram, four float4 loads in flight per thread
+#pragma unroll 1
+  for (int i0 = (int)team.tid; i0 < n4; i0 += 4 * NT) {
+    float4 a[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) a[q] = (i0 + q * NT < n4) ? row4[i0 + q * NT] : ninf4;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float xs[4] = {a[q].x, a[q].y, a[q].z, a[q].w};
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (xs[u] > -INFINITY) atomicAdd(&bs->hist[bin_of(xs[u])], 1u);
+    }
+  }
+  team.sync();
+  // 2. b*: thread t owns bins [t*PER, (t+1)*PER); suffix sums over threads
+  {
+    uint32_t c[PER], sum = 0;
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+      c[j] = bs->hist[team.tid * PER + j];
+      sum += c[j];
+    }
+    uint32_t incl = sum;  // suffix sum within the warp (lanes >= this one)
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const uint32_t x = __shfl_down_sync(0xFFFFFFFFu, incl, off);
+      if (lane + off < 32) incl += x;
+    }
+    if (lane == 0) bs->warp_sum[warp] = incl;
+    team.sync();
+    uint32_t higher = 0;  // entries in the bins of later warps
+    for (int w = (int)warp + 1; w < NW; ++w) higher += bs->warp_sum[w];
+    incl += higher;
+    const uint32_t excl = incl - sum;
+    if (excl < K && K <= incl) {
+      uint32_t acc = excl;
+#pragma unroll
+      for (int j = PER - 1; j >= 0; --j) {
+        if (acc < K && acc + c[j] >= K) {
+          bs->bcast[0] = team.tid * PER + (uint32_t)j;
+          bs->bcast[1] = acc;
+          bs->bcast[2] = c[j];
+          bs->bcast[3] = 0u;
+        }
+        acc += c[j];
+      }
+    }
+  }
+  team.sync();
+  const uint32_t bstar = bs->bcast[0], above = bs->bcast[1], m = bs->bcast[2];
+  if (m > (uint32_t)CAP) {
+    select_general<NT>(row, t0, n, K, 0u, 0u, true, out, sc, team.bar_id, team.tid);
+    return;
+  }
+  const uint32_t need = K - above;
+  // 3. bitmap of sure entries, per-segment counts, gather b*; two chunks in flight
+  const int seg_chunks = (chunks + NW - 1) / NW;
+  const int c_lo = min(chunks, (int)warp * seg_chunks);
+  const int c_hi = min(chunks, c_lo + seg_chunks);
+  uint32_t gt = 0;
+#pragma unroll 1
+  for (int c0 = c_lo; c0 < c_hi; c0 += 2) {
+    float4 v[2];
+#pragma unroll
+    for (int q = 0; q < 2; ++q) v[q] = (c0 + q < c_hi) ? row4[(c0 + q) * 32 + (int)lane] : ninf4;
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const int c = c0 + q;
+      const float xs[4] = {v[q].x, v[q].y, v[q].z, v[q].w};
+      uint32_t bal[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const bool vis = xs[u] > -INFINITY;
+        const uint32_t b = vis ? bin_of(xs[u]) : 0u;
+        const bool sure = vis && b > bstar;
+        bal[u] = __ballot_sync(0xFFFFFFFFu, sure);
+        gt += sure;
+        if (vis && b == bstar) {
+          const uint32_t slot = atomicAdd(&bs->bcast[3], 1u);
+          bs->cand[slot] = score_key(xs[u]);
+          bs->cand_t[slot] = (uint32_t)(c * 128 + 4 * (int)lane + u);  // relative to t0
+        }
+      }
+      if (lane == 0 && c < c_hi)
+        *reinterpret_cast<uint4*>(&bs->keep[4 * c]) = make_uint4(bal[0], bal[1], bal[2], bal[3]);
+    }
+  }
+  gt = __reduce_add_sync(0xFFFFFFFFu, gt);
+  if (lane == 0) bs->seg_gt[warp] = gt;
+  team.sync();
+  // 4. exact rank inside b*
+#pragma unroll 1
+  for (uint32_t i = team.tid; i < m; i += NT) {
+    const uint32_t ki = bs->cand[i], ti = bs->cand_t[i];
+    uint32_t rank = 0;
+#pragma unroll 4
+    for (uint32_t j = 0; j < m; ++j) {
+      const uint32_t kj = bs->cand[j], tj = bs->cand_t[j];
+      rank += (kj > ki) || (kj == ki && tj < ti);
+    }
+    if (rank < need) {
+      const uint32_t c = ti >> 7, l = (ti >> 2) & 31u, u = ti & 3u;
+      atomicOr(&bs->keep[4 * c + u], 1u << l);
+      atomicAdd(&bs->seg_sel[c / (uint32_t)seg_chunks], 1u);
+    }
+  }
+  team.sync();
+  // 5. ordered write from the bitmap
+  uint32_t base = 0, total = 0;
+  for (int w = 0; w < NW; ++w) {
+    const uint32_t cnt = bs->seg_gt[w] + bs->seg_sel[w];
+    base += (w < (int)warp) ? cnt : 0u;
+    total += cnt;
+  }
+  const uint32_t lt_mask = (1u << lane) - 1u;
+#pragma unroll 2
+  for (int c = c_lo; c < c_hi; ++c) {
+    const uint4 mw = *reinterpret_cast<const uint4*>(&bs->keep[4 * c]);
+    const uint32_t ms[4] = {mw.x, mw.y, mw.z, mw.w};
+    uint32_t pos = base;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) pos += __popc(ms[u] & lt_mask);
+    const int tb = t0 + c * 128 + 4 * (int)lane;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      if ((ms[u] >> lane) & 1u) {
+        if (pos < K) out[pos] = tb + u;
+        ++pos;
+      }
+    }
+    base += __popc(mw.x) + __popc(mw.y) + __popc(mw.z) + __popc(mw.w);
+  }
+  for (uint32_t i = min(total, K) + team.tid; i < K; i += NT) out[i] = -1;
+  team.sync();
 }
 
 }  // namespace csa
