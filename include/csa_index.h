@@ -103,6 +103,29 @@ csa_status csa_index_fused(const csa_problem* p, const void* q, const void* k, c
                            int32_t* idx, float* scores_dbg, void* workspace,
                            size_t workspace_bytes, void* stream);
 
+/* csa_index_fused without any caller workspace and without any allocation.
+ * The pages have no counterpart: this entry point exists for callers that
+ * cannot allocate device memory at the call site -- for instance a host
+ * process whose memory pool already owns (and has reserved) the free device
+ * memory, or a code path where the implicit device synchronisation of a
+ * cudaMalloc is not allowed.  Inputs and idx are as for csa_index_fused;
+ * the result equals csa_index_fused's for the same problem.
+ *  - Scores go through a scratch array compiled into the library (fp32,
+ *    at most 2,097,152 = 2^21 scores, i.e. 8 MiB: B*S*W must not exceed it,
+ *    e.g. 64 decode rows of 32768 entries).  Larger problems return
+ *    CSA_ERR_UNSUPPORTED before anything is launched.  Every GPU that loads
+ *    the library holds this array until the process exits.
+ *  - The first call on a device looks up the array's device address (once,
+ *    with that device current); make that first call before any stream
+ *    capture in the calling program.
+ *  - All calls share the one array: calls whose work overlaps on the GPU
+ *    (other streams, other host threads) race and corrupt each other's
+ *    results.  Each call writes every score it later reads, so nothing needs
+ *    clearing between calls.                                              */
+csa_status csa_index_fused_noalloc(const csa_problem* p, const void* q, const void* k, const void* w,
+                                   const int32_t* q_seg, const int32_t* kv_seg, const int64_t* q_start,
+                                   int32_t* idx, void* stream);
+
 /* Bytes of device workspace an entry point needs: which = 0 for
  * csa_index_topk, 1 for csa_index_fused.  Returns 0 when none is needed or
  * the problem is invalid.                                                 */

@@ -23,6 +23,7 @@ EXPORTED = (
     "csa_index_score",
     "csa_index_topk",
     "csa_index_fused",
+    "csa_index_fused_noalloc",
     "csa_index_workspace_size",
     "csa_index_device_status",
     "csa_index_selftest_timeout",
@@ -64,6 +65,7 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.csa_index_score.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp]
     lib.csa_index_topk.argtypes = [P, vp, vp, vp, sz, vp]
     lib.csa_index_fused.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.csa_index_fused_noalloc.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp]
     lib.csa_index_workspace_size.argtypes = [P, i32]
     lib.csa_index_workspace_size.restype = sz
     lib.csa_index_device_status.argtypes = [vp]
@@ -71,7 +73,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.csa_status_string.argtypes = [i32]
     lib.csa_status_string.restype = ctypes.c_char_p
     lib.csa_index_abi_version.restype = i32
-    for name in ("csa_index_score", "csa_index_topk", "csa_index_fused", "csa_index_device_status",
+    for name in ("csa_index_score", "csa_index_topk", "csa_index_fused", "csa_index_fused_noalloc",
+                 "csa_index_device_status",
                  "csa_index_selftest_timeout"):
         getattr(lib, name).restype = i32
     if path is None:
@@ -133,6 +136,12 @@ def index_fused_raw(p: Problem, q, k, w, q_seg, kv_seg, q_start, idx, scores_dbg
     return load().csa_index_fused(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(w), _ptr(q_seg), _ptr(kv_seg),
                                   _ptr(q_start), _ptr(idx), _ptr(scores_dbg), _ptr(workspace), nbytes,
                                   _stream(stream))
+
+
+def index_fused_noalloc_raw(p: Problem, q, k, w, q_seg, kv_seg, q_start, idx, stream=None) -> int:
+    """csa_index_fused_noalloc: no workspace, scores in the library's static scratch."""
+    return load().csa_index_fused_noalloc(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(w), _ptr(q_seg), _ptr(kv_seg),
+                                          _ptr(q_start), _ptr(idx), _stream(stream))
 
 
 def workspace_size(p: Problem, which: int) -> int:

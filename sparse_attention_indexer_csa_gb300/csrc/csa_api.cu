@@ -157,6 +157,35 @@ size_t fused_workspace_bytes(const csa_problem* p) {
   return (size_t)p->B * p->S * p->W * sizeof(float);
 }
 
+// ----------------------------------------------------------------- allocation-free variant
+// Scratch for csa_index_fused_noalloc: the fp32 scores of one call, at most
+// kNoAllocMaxScores of them (8 MiB).  Every GPU that loads the library keeps
+// this array until the process exits.  Host code must not use the symbol as
+// a pointer: noalloc_scratch() fetches its device address.
+constexpr size_t kNoAllocMaxScores = (size_t)2 * 1024 * 1024;
+static __device__ __align__(256) float g_noalloc_scores[kNoAllocMaxScores];
+
+// Device address of g_noalloc_scores on the current device, looked up once per
+// device (with that device current) and cached.
+float* noalloc_scratch(cudaError_t* err) {
+  constexpr int kMaxDevices = 64;
+  static std::once_flag flags[kMaxDevices];
+  static float* ptrs[kMaxDevices];
+  static cudaError_t errs[kMaxDevices];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    *err = cudaErrorInvalidDevice;
+    return nullptr;
+  }
+  std::call_once(flags[dev], [dev] {
+    void* ptr = nullptr;
+    errs[dev] = cudaGetSymbolAddress(&ptr, g_noalloc_scores);
+    ptrs[dev] = static_cast<float*>(ptr);
+  });
+  *err = errs[dev];
+  return errs[dev] == cudaSuccess ? ptrs[dev] : nullptr;
+}
+
 }  // namespace
 }  // namespace csa
 
@@ -213,6 +242,29 @@ csa_status csa_index_fused(const csa_problem* p, const void* q, const void* k, c
   st = run_index_kernel(p, false, q, k, w, q_seg, kv_seg, q_start, sc, nullptr, s);
   if (st != CSA_OK) return st;
   if (launch_topk(sc, idx, (long long)p->B * p->S, p->W, p->top_k, s) != cudaSuccess) return CSA_ERR_CUDA;
+  return CSA_OK;
+}
+
+csa_status csa_index_fused_noalloc(const csa_problem* p, const void* q, const void* k, const void* w,
+                                   const int32_t* q_seg, const int32_t* kv_seg, const int64_t* q_start,
+                                   int32_t* idx, void* stream) {
+  csa_status st = check_problem(p);
+  if (st != CSA_OK) return st;
+  if ((st = check_inputs(p, q, k, w, q_seg, kv_seg, q_start)) != CSA_OK) return st;
+  if (idx == nullptr || !aligned(idx, 4)) return CSA_ERR_INVALID_ARG;
+  if (!shape_supported(p)) return CSA_ERR_UNSUPPORTED;
+  if (p->W > kTopkMaxW) return CSA_ERR_UNSUPPORTED;
+  const size_t n_scores = (size_t)p->B * (size_t)p->S * (size_t)p->W;
+  if (n_scores > kNoAllocMaxScores) return CSA_ERR_UNSUPPORTED;  // beyond the library's static scratch
+  cudaError_t err = cudaSuccess;
+  float* scratch = noalloc_scratch(&err);
+  if (scratch == nullptr) return CSA_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // the score pass writes every entry the selection pass reads, so the
+  // scratch needs no clearing between calls
+  st = run_index_kernel(p, false, q, k, w, q_seg, kv_seg, q_start, scratch, nullptr, s);
+  if (st != CSA_OK) return st;
+  if (launch_topk(scratch, idx, (long long)p->B * p->S, p->W, p->top_k, s) != cudaSuccess) return CSA_ERR_CUDA;
   return CSA_OK;
 }
 
