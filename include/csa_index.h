@@ -92,12 +92,17 @@ csa_status csa_index_topk(const csa_problem* p, const float* scores, int32_t* id
                           void* workspace, size_t workspace_bytes, void* stream);
 
 /* Scores and selection in one call: same inputs as csa_index_score, writes
- * idx [B,S,top_k] int32.  For W <= 4096 the scores stay in on-chip memory
- * (never written to HBM) unless scores_dbg [B,S,W] fp32 is non-NULL, in
- * which case the exact fp32 scores the selection used are also written
- * there.  For larger W (decode-style problems) the scores go through
- * `workspace` (csa_index_workspace_size(p, 1) bytes, device memory owned by
- * the caller) and a second selection pass.                                */
+ * idx [B,S,top_k] int32.  Needs `workspace`: csa_index_workspace_size(p, 1)
+ * bytes of device memory owned by the caller (16-byte aligned).
+ *  - W <= 4096 and S > 2: one persistent kernel.  Each CTA stages the score
+ *    rows of its two most recent items of four rows in its slice of the
+ *    workspace (2 x 4 x W fp32 per CTA, at most 256 CTAs: a few tens of MB
+ *    that stay in L2), so the selection of one item overlaps the scores of
+ *    the next; the [B,S,W] score tensor is never formed.
+ *  - otherwise (decode-style single rows, long rows): the scores go to the
+ *    workspace ([B,S,W] fp32) and a second kernel selects.
+ * scores_dbg [B,S,W] fp32, if non-NULL, also receives the exact fp32 scores
+ * the selection used (every entry, -inf where masked).                    */
 csa_status csa_index_fused(const csa_problem* p, const void* q, const void* k, const void* w,
                            const int32_t* q_seg, const int32_t* kv_seg, const int64_t* q_start,
                            int32_t* idx, float* scores_dbg, void* workspace,
@@ -127,8 +132,8 @@ csa_status csa_index_fused_noalloc(const csa_problem* p, const void* q, const vo
                                    int32_t* idx, void* stream);
 
 /* Bytes of device workspace an entry point needs: which = 0 for
- * csa_index_topk, 1 for csa_index_fused.  Returns 0 when none is needed or
- * the problem is invalid.                                                 */
+ * csa_index_topk (always 0), 1 for csa_index_fused.  Depends only on the
+ * problem (no device query).  Returns 0 when the problem is invalid.      */
 size_t csa_index_workspace_size(const csa_problem* p, int32_t which);
 
 /* Synchronises `stream`, then reads and clears the device status word of

@@ -183,7 +183,7 @@ def index_fused(q, k, w, scale, compress_rate, top_k, q_seg=None, kv_seg=None, q
     if out is None:
         out = torch.empty(p.B, p.S, p.top_k, dtype=torch.int32, device=q.device)
     need = workspace_size(p, 1)
-    if need and workspace is None and scores_dbg is None:
+    if need and workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     _check("csa_index_fused", index_fused_raw(p, q, k, w, q_seg, kv_seg, q_start, out, scores_dbg,
                                               workspace, stream))

@@ -15,6 +15,7 @@ namespace csa {
 namespace {
 
 constexpr int kFusedMaxW = 4096;   // shared-memory score rows of the fused kernel
+constexpr int kMaxGrid = 256;      // CTAs of the persistent kernel (bounds the fused staging ring)
 constexpr int kTopkMaxW = 49152;   // one row staged in shared memory by the top-k kernel
 constexpr int kDecodeChunkTiles = 8;
 constexpr unsigned long long kWaitNs = 2000000000ull;  // 2 s per wait before giving up
@@ -51,7 +52,18 @@ bool shape_supported(const csa_problem* p) {
 // SM busy streaming k; everything else uses blocks of four query rows.
 bool use_row_kernel(const csa_problem* p) { return p->S <= 2 && p->H == 64 && p->D == 128; }
 
-bool fused_in_smem(const csa_problem* p) { return !use_row_kernel(p) && p->W <= kFusedMaxW; }
+// Fused in one kernel (selection on the SM) unless the problem is single-row
+// or its rows are too long for shared memory; those go through two passes.
+bool fused_one_kernel(const csa_problem* p) { return !use_row_kernel(p) && p->W <= kFusedMaxW; }
+
+int w_pad_of(const csa_problem* p) { return ((p->W + kTileT - 1) / kTileT) * kTileT; }
+
+// Staging ring of the one-kernel fused path: two items of four rows per CTA.
+size_t fused_ring_bytes(const csa_problem* p) {
+  const long long items = (long long)p->B * ((p->S + 3) / 4);
+  const long long ctas = std::min<long long>(items, kMaxGrid);
+  return (size_t)ctas * 2 * 4 * (size_t)w_pad_of(p) * sizeof(float);
+}
 
 int num_sms() {
   static int cached[64];
@@ -114,7 +126,7 @@ bool make_k_map(CUtensorMap* m, const csa_problem* p, const void* k) {
 
 csa_status run_index_kernel(const csa_problem* p, bool fused, const void* q, const void* k, const void* w,
                             const int32_t* q_seg, const int32_t* kv_seg, const int64_t* q_start, float* scores,
-                            int32_t* idx, cudaStream_t stream) {
+                            int32_t* idx, float* ring, cudaStream_t stream) {
   const bool row_kernel = use_row_kernel(p);
   KernelChoice kc{p->H, p->D, row_kernel ? 1 : 4, fused};
   CUtensorMap tq, tk;
@@ -134,6 +146,7 @@ csa_status run_index_kernel(const csa_problem* p, bool fused, const void* q, con
   kp.q_start = q_start;
   kp.scores = scores;
   kp.idx = idx;
+  kp.ring = ring;
   kp.n_rb = (p->S + kc.R - 1) / kc.R;
   kp.n_tiles = (p->W + kTileT - 1) / kTileT;
   kp.chunk_tiles = row_kernel ? std::min(kp.n_tiles, kDecodeChunkTiles) : kp.n_tiles;
@@ -147,13 +160,14 @@ csa_status run_index_kernel(const csa_problem* p, bool fused, const void* q, con
   if (index_kernel_smem(kc, kp.w_pad) > 227u * 1024u) return CSA_ERR_UNSUPPORTED;
   const int sms = num_sms();
   if (sms <= 0) return CSA_ERR_CUDA;
-  const int grid = (int)std::min<long long>(items, sms);
+  const int grid = (int)std::min<long long>(items, std::min(sms, kMaxGrid));
   if (launch_index_kernel(kc, tq, tk, kp, grid, stream) != cudaSuccess) return CSA_ERR_CUDA;
   return CSA_OK;
 }
 
 size_t fused_workspace_bytes(const csa_problem* p) {
-  if (check_problem(p) != CSA_OK || fused_in_smem(p)) return 0;
+  if (check_problem(p) != CSA_OK) return 0;
+  if (fused_one_kernel(p)) return fused_ring_bytes(p);
   return (size_t)p->B * p->S * p->W * sizeof(float);
 }
 
@@ -201,7 +215,7 @@ csa_status csa_index_score(const csa_problem* p, const void* q, const void* k, c
   if ((st = check_inputs(p, q, k, w, q_seg, kv_seg, q_start)) != CSA_OK) return st;
   if (scores == nullptr || !aligned(scores, 4)) return CSA_ERR_INVALID_ARG;
   if (!shape_supported(p)) return CSA_ERR_UNSUPPORTED;
-  return run_index_kernel(p, false, q, k, w, q_seg, kv_seg, q_start, scores, nullptr,
+  return run_index_kernel(p, false, q, k, w, q_seg, kv_seg, q_start, scores, nullptr, nullptr,
                           static_cast<cudaStream_t>(stream));
 }
 
@@ -229,17 +243,21 @@ csa_status csa_index_fused(const csa_problem* p, const void* q, const void* k, c
   if (scores_dbg != nullptr && !aligned(scores_dbg, 4)) return CSA_ERR_INVALID_ARG;
   if (!shape_supported(p)) return CSA_ERR_UNSUPPORTED;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (fused_in_smem(p)) return run_index_kernel(p, true, q, k, w, q_seg, kv_seg, q_start, scores_dbg, idx, s);
-  // Large W: scores pass through the caller's workspace, then a selection pass.
-  if (p->W > kTopkMaxW) return CSA_ERR_UNSUPPORTED;
   const size_t need = fused_workspace_bytes(p);
+  if (fused_one_kernel(p)) {
+    if (workspace == nullptr || workspace_bytes < need || !aligned(workspace, 16)) return CSA_ERR_INVALID_ARG;
+    return run_index_kernel(p, true, q, k, w, q_seg, kv_seg, q_start, scores_dbg, idx,
+                            static_cast<float*>(workspace), s);
+  }
+  // Long rows or single-row problems: scores through the workspace (or the
+  // caller's debug copy), then the selection kernel.
+  if (p->W > kTopkMaxW) return CSA_ERR_UNSUPPORTED;
   float* sc = scores_dbg;
   if (sc == nullptr) {
-    if (workspace == nullptr || workspace_bytes < need) return CSA_ERR_INVALID_ARG;
-    if (!aligned(workspace, 16)) return CSA_ERR_INVALID_ARG;
+    if (workspace == nullptr || workspace_bytes < need || !aligned(workspace, 16)) return CSA_ERR_INVALID_ARG;
     sc = static_cast<float*>(workspace);
   }
-  st = run_index_kernel(p, false, q, k, w, q_seg, kv_seg, q_start, sc, nullptr, s);
+  st = run_index_kernel(p, false, q, k, w, q_seg, kv_seg, q_start, sc, nullptr, nullptr, s);
   if (st != CSA_OK) return st;
   if (launch_topk(sc, idx, (long long)p->B * p->S, p->W, p->top_k, s) != cudaSuccess) return CSA_ERR_CUDA;
   return CSA_OK;
@@ -262,7 +280,7 @@ csa_status csa_index_fused_noalloc(const csa_problem* p, const void* q, const vo
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // the score pass writes every entry the selection pass reads, so the
   // scratch needs no clearing between calls
-  st = run_index_kernel(p, false, q, k, w, q_seg, kv_seg, q_start, scratch, nullptr, s);
+  st = run_index_kernel(p, false, q, k, w, q_seg, kv_seg, q_start, scratch, nullptr, nullptr, s);
   if (st != CSA_OK) return st;
   if (launch_topk(scratch, idx, (long long)p->B * p->S, p->W, p->top_k, s) != cudaSuccess) return CSA_ERR_CUDA;
   return CSA_OK;

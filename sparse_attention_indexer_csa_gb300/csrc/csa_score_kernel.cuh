@@ -15,16 +15,20 @@
 // accumulation instead of the [B,H,S,W] tensor) with the masks of "DSV4: Add
 // indexer_save_selection and indexer_sharded_topk" (mask review hunk).
 //
-// Warp roles (block = 4 control warps + EW epilogue warps):
+// Warp roles (block = 4 control warps + EW epilogue warps [+ R select warps]):
 //   warp 0  TMA producer: q block per item, k tiles into a ring of stages
 //   warp 1  TMEM owner and UMMA issuer (one elected thread)
 //   warps 2, 3  schedulers (alternate items): per item compute the visible
 //           tile range, per-row thresholds / segment ids / visible counts and
 //           stage the weights into a ring of item slots
 //   warps 4..4+EW-1  epilogue (warp w reads TMEM lanes 32*(w%4) ..)
-// FUSED: scores stay in shared memory ([R][W] fp32) together with per-row
-// visible counts and value ranges, and the epilogue warps then run the
-// per-row selection, two warps per row.
+//   FUSED: warps 4+EW .. 4+EW+R-1  select warps, one query row each.
+// FUSED: the epilogue writes each item's R score rows into one of two
+// per-CTA staging slots in the caller's workspace (2 x R x W fp32 per CTA,
+// small enough to stay in L2) and folds per-row min / max / visible counts
+// into shared memory; the select warps pull the item's rows into shared
+// memory with one bulk copy, free the slot and select, so the selection of
+// item i runs while the tensor cores and the epilogue work on item i+1.
 //
 // Tiles wholly past the rows' future-mask bound, or (with segment ids)
 // outside the range of entries sharing a segment with the item's rows, are
@@ -48,6 +52,7 @@ struct KParams {
   const int64_t* q_start;
   float* scores;  // score mode: output; fused: optional debug copy
   int32_t* idx;   // fused: selection output
+  float* ring;    // fused: per-CTA staging of two items' score rows [grid][2][R][w_pad]
   int n_rb, n_tiles, n_chunks, chunk_tiles, n_items;
   int w_pad;  // fused: row pitch (floats) of the shared score rows
   unsigned long long wait_ns;
@@ -66,7 +71,7 @@ struct ItemDesc {
   int contig[R];   // the row's visible entries are tfirst .. tfirst + nvis - 1
 };
 
-// Selection scratch of one row team of the fused kernel.
+// Selection scratch of one select warp of the fused kernel.
 struct FusedRowScratch {
   SelectScratch sc;
   BinScratch<512, 256, 128> bs;  // rows of up to 4096 entries
@@ -90,12 +95,12 @@ struct Cfg {
   static_assert(D % 32 == 0, "head dim must be a multiple of 32");
   static constexpr int KSTAGES = (R == 1) ? 5 : 2;
   static constexpr int QBUF = FUSED ? 1 : 2;
-  static constexpr int SLOTS = 4;                  // item ring depth
+  static constexpr int SLOTS = FUSED ? 6 : 4;      // item ring depth
   static constexpr int EW = (R >= 2) ? 8 : 4;      // epilogue warps
+  static constexpr int SW = FUSED ? R : 0;         // select warps (one row each)
   static constexpr int RW = (R >= 2) ? R / 2 : 1;  // rows per epilogue warp
   static_assert(R == 1 || R % 2 == 0, "R must be 1 or even");
-  static_assert(!FUSED || R == 4, "the fused selection runs two warps on each of four rows");
-  static constexpr int NTHREADS = 128 + EW * 32;
+  static constexpr int NTHREADS = 128 + (EW + SW) * 32;
   static constexpr uint32_t QCHUNK = N * ROWB;       // bytes of one K-chunk of the q block
   static constexpr uint32_t KCHUNK = kTileT * ROWB;  // bytes of one K-chunk of a k tile
   static constexpr uint32_t QBYTES = QCHUNK * NKC;
@@ -109,12 +114,12 @@ struct Cfg {
   static constexpr uint32_t OFF_DESC = OFF_W + SLOTS * R * H * 4;
   static constexpr uint32_t OFF_BAR = (OFF_DESC + SLOTS * sizeof(ItemDesc<R>) + 15) & ~15u;
   // barriers: item_full[SLOTS], item_empty[SLOTS], q_full[QB], q_empty[QB], k_full[KS], k_empty[KS],
-  //           acc_full[2], acc_empty[2], drain
-  static constexpr int NBAR = 2 * SLOTS + 2 * QBUF + 2 * KSTAGES + 4 + 1;
+  //           acc_full[2], acc_empty[2], drain, ring_full[2], ring_empty[2], copy_full
+  static constexpr int NBAR = 2 * SLOTS + 2 * QBUF + 2 * KSTAGES + 4 + 1 + 5;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;  // tmem base, abort flag
-  static constexpr uint32_t OFF_STATS = (OFF_MISC + 16 + 15) & ~15u;  // RowStats[R]
-  static constexpr uint32_t OFF_SCR = (OFF_STATS + R * sizeof(RowStats) + 15) & ~15u;
-  static constexpr uint32_t NSCR = FUSED ? R : 0;
+  static constexpr uint32_t OFF_STATS = (OFF_MISC + 16 + 15) & ~15u;  // RowStats[2][R]
+  static constexpr uint32_t OFF_SCR = (OFF_STATS + 2 * R * sizeof(RowStats) + 15) & ~15u;
+  static constexpr uint32_t NSCR = SW;
   static constexpr uint32_t OFF_SROW = (OFF_SCR + NSCR * sizeof(FusedRowScratch) + 127) & ~127u;
   // dynamic shared memory for a given fused row pitch (+1 KB alignment slack)
   static constexpr uint32_t smem_bytes(int w_pad) {
@@ -144,11 +149,16 @@ struct Smem {
   __device__ uint64_t* acc_full(int i) const { return bar(B2 + i); }
   __device__ uint64_t* acc_empty(int i) const { return bar(B2 + 2 + i); }
   __device__ uint64_t* drain() const { return bar(B2 + 4); }
+  __device__ uint64_t* ring_full(int i) const { return bar(B2 + 5 + i); }
+  __device__ uint64_t* ring_empty(int i) const { return bar(B2 + 7 + i); }
+  __device__ uint64_t* copy_full() const { return bar(B2 + 9); }
   __device__ uint32_t* tmem_slot() const { return reinterpret_cast<uint32_t*>(base + C::OFF_MISC); }
   __device__ volatile uint32_t* abort_flag() const {
     return reinterpret_cast<volatile uint32_t*>(base + C::OFF_MISC + 4);
   }
-  __device__ RowStats* stats(int j) const { return reinterpret_cast<RowStats*>(base + C::OFF_STATS) + j; }
+  __device__ RowStats* stats(int slot, int j) const {
+    return reinterpret_cast<RowStats*>(base + C::OFF_STATS) + slot * C::R + j;
+  }
   __device__ FusedRowScratch* scratch(int j) const {
     return reinterpret_cast<FusedRowScratch*>(base + C::OFF_SCR) + j;
   }
@@ -486,14 +496,18 @@ __device__ void run_epilogue(const KParams& p, const Smem<C>& sm, const WaitCtl&
   const int hf = (C::EW == 8) ? (e / 4) : 0;
   const bool segs = p.q_seg != nullptr;
   const uint32_t t_lane = tmem_base + ((uint32_t)(quarter * 32) << 16);
-  uint32_t acount = 0;
+  uint32_t acount = 0, nt = 0;
   int it = 0;
   for (int item = blockIdx.x; item < p.n_items; item += gridDim.x, ++it) {
     const int slot = it % C::SLOTS;
     mbar_wait(sm.item_full(slot), (it / C::SLOTS) & 1, ctl);
     const ItemDesc<R>* d = sm.desc(slot);
     const int b = d->b, s0 = d->s0, t_lo = d->t_lo, t_hi = d->t_hi, c_lo = d->c_lo, c_hi = d->c_hi;
-    const int trivial = d->trivial;
+    if (C::FUSED && d->trivial) {  // the select warps write the visible sets
+      __syncwarp();
+      if (lane == 0) mbar_arrive(sm.item_empty(slot));
+      continue;
+    }
     int thr[RW], seg[RW];
     float smin[RW], smax[RW];
     uint32_t scnt[RW];
@@ -506,6 +520,12 @@ __device__ void run_epilogue(const KParams& p, const Smem<C>& sm, const WaitCtl&
       scnt[jj] = 0u;
     }
     const float* ws = sm.w(slot);
+    float* ring_rows = nullptr;  // this item's staging slot (fused)
+    const int rs = (int)(nt & 1u);
+    if constexpr (C::FUSED) {
+      mbar_wait(sm.ring_empty(rs), ((nt >> 1) & 1u) ^ 1u, ctl);
+      ring_rows = p.ring + ((size_t)blockIdx.x * 2 + rs) * R * p.w_pad;
+    }
     const bool write_all = !C::FUSED || p.scores != nullptr;
     const int tile_begin = write_all ? c_lo : t_lo;
     const int tile_end = write_all ? c_hi : t_hi;
@@ -534,7 +554,7 @@ __device__ void run_epilogue(const KParams& p, const Smem<C>& sm, const WaitCtl&
         const bool vis = computed && t < thr[jj] && (!segs || kvs == seg[jj]);
         const float val = vis ? p.scale * acc[jj] : -INFINITY;
         if constexpr (C::FUSED) {
-          if (t < p.w_pad) sm.srow(j, p.w_pad)[t] = val;
+          if (computed) ring_rows[(size_t)j * p.w_pad + t] = val;
           if (vis) {
             smin[jj] = fminf(smin[jj], val);
             smax[jj] = fmaxf(smax[jj], val);
@@ -544,44 +564,81 @@ __device__ void run_epilogue(const KParams& p, const Smem<C>& sm, const WaitCtl&
         if (p.scores != nullptr && s < p.S && t < p.W) p.scores[((size_t)b * p.S + s) * p.W + t] = val;
       }
     }
-    if constexpr (C::FUSED) {
-      if (!trivial) {  // fold this warp's row statistics into the shared per-row ones
+    if constexpr (C::FUSED) {  // row statistics, then hand the slot to the select warps
 #pragma unroll
-        for (int jj = 0; jj < RW; ++jj) {
-          const uint32_t cnt = __reduce_add_sync(0xFFFFFFFFu, scnt[jj]);
-          const uint32_t kmin = __reduce_min_sync(0xFFFFFFFFu, score_key(smin[jj]));
-          const uint32_t kmax = __reduce_max_sync(0xFFFFFFFFu, score_key(smax[jj]));
-          if (lane == 0 && cnt > 0u) {
-            RowStats* st = sm.stats(hf * RW + jj);
-            atomicAdd(&st->nvis, cnt);
-            atomicMin(&st->min_key, kmin);
-            atomicMax(&st->max_key, kmax);
-          }
+      for (int jj = 0; jj < RW; ++jj) {
+        const uint32_t cnt = __reduce_add_sync(0xFFFFFFFFu, scnt[jj]);
+        const uint32_t kmin = __reduce_min_sync(0xFFFFFFFFu, score_key(smin[jj]));
+        const uint32_t kmax = __reduce_max_sync(0xFFFFFFFFu, score_key(smax[jj]));
+        if (lane == 0 && cnt > 0u) {
+          RowStats* st = sm.stats(rs, hf * RW + jj);
+          atomicAdd(&st->nvis, cnt);
+          atomicMin(&st->min_key, kmin);
+          atomicMax(&st->max_key, kmax);
         }
       }
-      named_bar_sync(1, C::EW * 32);  // the item's scores and row statistics are in shared memory
-      const int j = e / 2;            // two warps per row
-      const int s = s0 + j;
-      const Team<64> team{(uint32_t)(2 + j), (uint32_t)((e & 1) * 32) + lane};
-      if (s < p.S) {
-        int32_t* out = p.idx + ((size_t)b * p.S + s) * p.K;
-        FusedRowScratch* fs = sm.scratch(j);
-        if (trivial) {
-          write_visible_set<64>(out, p.K, d->nvis[j], d->tfirst[j], d->contig[j], d->thr[j], d->seg[j],
-                                p.kv_seg + (size_t)b * p.W, &fs->sc, team);
-        } else {
-          const RowStats st = *sm.stats(j);
-          team_topk_row(sm.srow(j, p.w_pad), t_lo * kTileT, (t_hi - t_lo) * kTileT, (uint32_t)p.K, st, out,
-                        &fs->bs, &fs->sc, team);
-          if (team.tid == 0) {
-            RowStats* w = sm.stats(j);
-            w->nvis = 0u;
-            w->min_key = 0xFFFFFFFFu;
-            w->max_key = 0u;
-          }
-        }
+      fence_proxy_async_global();  // the staged rows are read back by a bulk copy
+      __syncwarp();
+      if (lane == 0) mbar_arrive(sm.ring_full(rs));
+      ++nt;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(sm.item_empty(slot));
+  }
+}
+
+// Select warp `j` (fused): selection of row j of every item.  Trivial items
+// keep every visible entry; the others wait for their staged score rows,
+// which one thread copies into shared memory for all R rows at once.
+template <class C>
+__device__ void run_selector(const KParams& p, const Smem<C>& sm, const WaitCtl& ctl, int j) {
+  constexpr int R = C::R;
+  constexpr uint32_t kSelBar = 6;  // named barrier of the select warps
+  const uint32_t lane = lane_id();
+  const Team<32> team{0u, lane};
+  FusedRowScratch* fs = sm.scratch(j);
+  uint32_t nt = 0;
+  int it = 0;
+  for (int item = blockIdx.x; item < p.n_items; item += gridDim.x, ++it) {
+    const int slot = it % C::SLOTS;
+    mbar_wait(sm.item_full(slot), (it / C::SLOTS) & 1, ctl);
+    const ItemDesc<R>* d = sm.desc(slot);
+    const int b = d->b, s0 = d->s0, s = s0 + j;
+    int32_t* out = p.idx + ((size_t)b * p.S + s) * p.K;
+    if (d->trivial) {
+      if (s < p.S)
+        write_visible_set<32>(out, p.K, d->nvis[j], d->tfirst[j], d->contig[j], d->thr[j], d->seg[j],
+                              p.kv_seg + (size_t)b * p.W, &fs->sc, team);
+    } else {
+      const int rs = (int)(nt & 1u);
+      const int t_lo = d->t_lo, t_hi = d->t_hi;
+      const int e0 = t_lo * kTileT;
+      const uint32_t row_bytes = (uint32_t)(t_hi - t_lo) * kTileT * 4u;
+      mbar_wait(sm.ring_full(rs), (nt >> 1) & 1u, ctl);
+      if (j == 0 && lane == 0) {
+        fence_proxy_async_global();
+        const float* src = p.ring + ((size_t)blockIdx.x * 2 + rs) * R * p.w_pad;
+        mbar_arrive_expect_tx(sm.copy_full(), row_bytes * R);
+        if (row_bytes > 0u)
+          for (int r = 0; r < R; ++r)
+            bulk_copy_g2s(sm.srow(r, p.w_pad) + e0, src + (size_t)r * p.w_pad + e0, row_bytes, sm.copy_full());
       }
-      named_bar_sync(1, C::EW * 32);  // shared score rows and statistics may be overwritten
+      mbar_wait(sm.copy_full(), nt & 1u, ctl);
+      RowStats* stp = sm.stats(rs, j);
+      const RowStats st = *stp;
+      __syncwarp();
+      if (lane == 0) {
+        stp->nvis = 0u;
+        stp->min_key = 0xFFFFFFFFu;
+        stp->max_key = 0u;
+      }
+      named_bar_sync(kSelBar, 32 * R);  // every select warp holds its statistics
+      if (j == 0 && lane == 0) mbar_arrive(sm.ring_empty(rs));
+      if (s < p.S)
+        team_topk_row(sm.srow(j, p.w_pad), e0, (t_hi - t_lo) * kTileT, (uint32_t)p.K, st, out, &fs->bs, &fs->sc,
+                      team);
+      named_bar_sync(kSelBar, 32 * R);  // the shared rows may be refilled
+      ++nt;
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(sm.item_empty(slot));
@@ -601,7 +658,7 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::SLOTS; ++s) {
       mbar_init(sm.item_full(s), 1);
-      mbar_init(sm.item_empty(s), 2 + C::EW);
+      mbar_init(sm.item_empty(s), 2 + C::EW + C::SW);
     }
     for (int i = 0; i < C::QBUF; ++i) {
       mbar_init(sm.q_full(i), 1);
@@ -616,11 +673,17 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
       mbar_init(sm.acc_empty(i), C::EW);
     }
     mbar_init(sm.drain(), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(sm.ring_full(i), C::EW);
+      mbar_init(sm.ring_empty(i), 1);
+    }
+    mbar_init(sm.copy_full(), 1);
     *sm.abort_flag() = 0u;
-    for (int j = 0; j < C::R; ++j) {
-      sm.stats(j)->nvis = 0u;
-      sm.stats(j)->min_key = 0xFFFFFFFFu;
-      sm.stats(j)->max_key = 0u;
+    for (int i = 0; i < 2 * C::R; ++i) {
+      RowStats* st = sm.stats(i / C::R, i % C::R);
+      st->nvis = 0u;
+      st->min_key = 0xFFFFFFFFu;
+      st->max_key = 0u;
     }
     fence_mbar_init();
   }
@@ -644,8 +707,10 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
     if (lane == 0) run_mma<C>(p, sm, ctl, tmem_base);
   } else if (warp == 2 || warp == 3) {
     run_scheduler<C>(p, sm, ctl, warp - 2);
-  } else {
+  } else if (warp < 4 + C::EW) {
     run_epilogue<C>(p, sm, ctl, tmem_base, warp - 4);
+  } else {
+    if constexpr (C::FUSED) run_selector<C>(p, sm, ctl, warp - 4 - C::EW);
   }
   __syncwarp();
   tc_fence_before();
