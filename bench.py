@@ -36,6 +36,10 @@ from csa_inputs import WORKLOADS, Inputs, make_inputs  # noqa: E402
 
 METRIC = "indexer useful TFLOP/s and query rows/s at S=16K; % of bf16 tensor peak"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# DRAM bytes (read + write) per launch of the timed kernel, from the ncu launch
+# list summarised in profiles/ (fused_prefill_16k_launches.md).  Reset an
+# entry to None whenever that kernel changes.
+MEASURED_TRAFFIC = {"prefill_16k": 274.95e6 + 223.9e6}
 
 
 # ----------------------------------------------------------------------------- work accounting
@@ -346,7 +350,7 @@ def run_ours(args, wl, inp):
     achieved = wk["flops_nontrivial"] / (avg_launch_ms * 1e-3) / 1e12
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     bound, unit = "tensor", "TFLOP/s"
-    traffic = None
+    traffic = MEASURED_TRAFFIC.get(wl.name) if args.batch is None else None
     if wl.name.startswith("decode"):
         # k streaming bound: algorithmic bytes = k + q + w + scores write/read + idx
         bytes_alg = (wl.B * wl.W * wl.D * 2 + wl.B * wl.H * wl.S * wl.D * 2 + wl.B * wl.S * wl.H * 2
