@@ -133,7 +133,8 @@ cudaError_t launch_topk_nt(const float* scores, int32_t* idx, long long rows, in
 int topk_threads(int W) {
   if (W <= 2048) return 128;
   if (W <= 8192) return 256;
-  return 512;
+  if (W <= 16384) return 512;
+  return 1024;
 }
 
 cudaError_t launch_topk(const float* scores, int32_t* idx, long long rows, int W, int K, cudaStream_t stream) {
@@ -141,7 +142,8 @@ cudaError_t launch_topk(const float* scores, int32_t* idx, long long rows, int W
   switch (topk_threads(W)) {
     case 128: return launch_topk_nt<128>(scores, idx, rows, W, K, stream);
     case 256: return launch_topk_nt<256>(scores, idx, rows, W, K, stream);
-    default: return launch_topk_nt<512>(scores, idx, rows, W, K, stream);
+    case 512: return launch_topk_nt<512>(scores, idx, rows, W, K, stream);
+    default: return launch_topk_nt<1024>(scores, idx, rows, W, K, stream);
   }
 }
 
