@@ -57,22 +57,33 @@ typedef enum {
 
 typedef enum { CSA_BF16 = 0, CSA_F32 = 1 } csa_dtype;
 
+/* Layout of q: head-major [B,H,S,D] (the pages' kernel layout) or
+ * sequence-major [B,S,H,D] (the layout the pages' RoPE produces, used to
+ * avoid transposes).                                                      */
+typedef enum { CSA_Q_HEAD_MAJOR = 0, CSA_Q_SEQ_MAJOR = 1 } csa_q_layout;
+
 /* Problem description (all sizes in elements).
  *   B  batch, H indexer heads, S query rows per batch, D head dim,
  *   W  compressed entries per batch (the compressed KV length),
  *   compress_rate  tokens per compressed entry (>= 1),
  *   scale  > 0, applied to q.k inside the ReLU (e.g. D^-0.5),
  *   top_k  >= 1 (may exceed the visible count or W: -1 padding),
- *   w_dtype  storage type of the weights (csa_dtype).               */
+ *   w_dtype  storage type of the weights (csa_dtype),
+ *   q_layout  csa_q_layout of q (added in ABI version 101).
+ * A decode batch with sequences of different lengths shares one k buffer
+ * [B,W,D] sized for the longest; q_start[b] (the row's position) bounds
+ * each sequence's visible entries, so entries past a sequence's length are
+ * never selected and their tiles are never multiplied.                  */
 typedef struct {
   int32_t B, H, S, D, W;
   int32_t compress_rate;
   float scale;
   int32_t top_k;
   int32_t w_dtype;
+  int32_t q_layout;
 } csa_problem;
 
-/* Scores.  q [B,H,S,D] bf16, k [B,W,D] bf16, w [B,S,H] (w_dtype),
+/* Scores.  q [B,H,S,D] (or [B,S,H,D], q_layout) bf16, k [B,W,D] bf16, w [B,S,H] (w_dtype),
  * q_seg [B,S] int32 or NULL, kv_seg [B,W] int32 or NULL (both or neither),
  * q_start [B] int64 or NULL.  Writes scores [B,S,W] fp32, -inf where masked.
  * Defined by the score formula above ("Add StreamIndex Kernel for CSA
@@ -107,6 +118,16 @@ csa_status csa_index_fused(const csa_problem* p, const void* q, const void* k, c
                            const int32_t* q_seg, const int32_t* kv_seg, const int64_t* q_start,
                            int32_t* idx, float* scores_dbg, void* workspace,
                            size_t workspace_bytes, void* stream);
+
+/* Gather of the selected compressed entries, the rows sparse attention reads
+ * ("DSV4: Add indexer_save_selection and indexer_sharded_topk", Description:
+ * the selection is handed to sparse attention in sequence layout):
+ *   out[b,s,i,:] = k[b, idx[b,s,i], :],  zeros where idx[b,s,i] == -1.
+ * k [B,W,D] bf16, idx [B,S,top_k] int32 (a selection from this library or
+ * any int32 indices), out [B,S,top_k,D] bf16; uses B, S, W, D, top_k of p.
+ * An index outside [-1, W) writes a zero row and records CSA_ERR_DEVICE in
+ * the device status word.  Supported: D in {32, 128}.                    */
+csa_status csa_index_gather(const csa_problem* p, const void* k, const int32_t* idx, void* out, void* stream);
 
 /* csa_index_fused without any caller workspace and without any allocation.
  * The pages have no counterpart: this entry point exists for callers that

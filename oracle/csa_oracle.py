@@ -150,6 +150,20 @@ def index_topk(q, k, w, scale, compress_rate, top_k, q_start=None, q_seg=None,
     return sc, select_topk(sc, top_k)
 
 
+def gather_selected(k, idx) -> np.ndarray:
+    """``out[b,s,i,:] = k[b, idx[b,s,i], :]``, zeros where ``idx == -1``: the
+    selected compressed rows handed to sparse attention ("DSV4: Add
+    indexer_save_selection and indexer_sharded_topk", Description)."""
+    K = np.asarray(k)
+    I = np.asarray(idx)
+    B, W, D = K.shape
+    out = np.zeros(I.shape + (D,), dtype=K.dtype)
+    for b in range(B):
+        sel = I[b] >= 0
+        out[b][sel] = K[b][I[b][sel]]
+    return out
+
+
 def visible_counts(B, S, W, compress_rate, q_start=None, q_seg=None, kv_seg=None, rows=None):
     """``v[b,s]``: number of visible entries of each row."""
     return visibility(B, S, W, compress_rate, q_start, q_seg, kv_seg, rows).sum(axis=-1)

@@ -18,12 +18,14 @@ LIB_PATH = os.path.join(_PKG, "libcsa_index.so")
 
 CSA_OK, CSA_ERR_INVALID_ARG, CSA_ERR_UNSUPPORTED, CSA_ERR_CUDA, CSA_ERR_TIMEOUT, CSA_ERR_DEVICE = range(6)
 CSA_BF16, CSA_F32 = 0, 1
+CSA_Q_HEAD_MAJOR, CSA_Q_SEQ_MAJOR = 0, 1
 
 EXPORTED = (
     "csa_index_score",
     "csa_index_topk",
     "csa_index_fused",
     "csa_index_fused_noalloc",
+    "csa_index_gather",
     "csa_index_workspace_size",
     "csa_index_device_status",
     "csa_index_selftest_timeout",
@@ -45,6 +47,7 @@ class Problem(ctypes.Structure):
         ("B", ctypes.c_int32), ("H", ctypes.c_int32), ("S", ctypes.c_int32),
         ("D", ctypes.c_int32), ("W", ctypes.c_int32), ("compress_rate", ctypes.c_int32),
         ("scale", ctypes.c_float), ("top_k", ctypes.c_int32), ("w_dtype", ctypes.c_int32),
+        ("q_layout", ctypes.c_int32),
     ]
 
 
@@ -66,6 +69,7 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.csa_index_topk.argtypes = [P, vp, vp, vp, sz, vp]
     lib.csa_index_fused.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     lib.csa_index_fused_noalloc.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp]
+    lib.csa_index_gather.argtypes = [P, vp, vp, vp, vp]
     lib.csa_index_workspace_size.argtypes = [P, i32]
     lib.csa_index_workspace_size.restype = sz
     lib.csa_index_device_status.argtypes = [vp]
@@ -73,7 +77,7 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.csa_status_string.argtypes = [i32]
     lib.csa_status_string.restype = ctypes.c_char_p
     lib.csa_index_abi_version.restype = i32
-    for name in ("csa_index_score", "csa_index_topk", "csa_index_fused", "csa_index_fused_noalloc",
+    for name in ("csa_index_score", "csa_index_topk", "csa_index_fused", "csa_index_fused_noalloc", "csa_index_gather",
                  "csa_index_device_status",
                  "csa_index_selftest_timeout"):
         getattr(lib, name).restype = i32
@@ -109,13 +113,17 @@ def _stream(stream) -> ctypes.c_void_p:
 
 
 def make_problem(q: torch.Tensor, k: torch.Tensor, w: torch.Tensor, scale: float, compress_rate: int,
-                 top_k: int = 1) -> Problem:
-    B, H, S, D = q.shape
+                 top_k: int = 1, q_layout: int = CSA_Q_HEAD_MAJOR) -> Problem:
+    """Problem of q [B,H,S,D] (head-major) or q [B,S,H,D] (q_layout=CSA_Q_SEQ_MAJOR)."""
+    if q_layout == CSA_Q_SEQ_MAJOR:
+        B, S, H, D = q.shape
+    else:
+        B, H, S, D = q.shape
     W = k.shape[1]
     wd = {torch.bfloat16: CSA_BF16, torch.float32: CSA_F32}.get(w.dtype)
     if wd is None:
         raise ValueError("weights must be bf16 or fp32")
-    return Problem(B, H, S, D, W, int(compress_rate), float(scale), int(top_k), wd)
+    return Problem(B, H, S, D, W, int(compress_rate), float(scale), int(top_k), wd, int(q_layout))
 
 
 # ----------------------------------------------------------------------------- raw C-ABI calls
@@ -157,9 +165,10 @@ def selftest_timeout(timeout_us: int, stream=None) -> int:
 
 
 # ----------------------------------------------------------------------------- tensor-level helpers
-def index_score(q, k, w, scale, compress_rate, q_seg=None, kv_seg=None, q_start=None, out=None, stream=None):
+def index_score(q, k, w, scale, compress_rate, q_seg=None, kv_seg=None, q_start=None, out=None, stream=None,
+                q_layout=CSA_Q_HEAD_MAJOR):
     """Scores [B,S,W] fp32 (-inf where masked) on the GPU."""
-    p = make_problem(q, k, w, scale, compress_rate)
+    p = make_problem(q, k, w, scale, compress_rate, 1, q_layout)
     if out is None:
         out = torch.empty(p.B, p.S, p.W, dtype=torch.float32, device=q.device)
     _check("csa_index_score", index_score_raw(p, q, k, w, q_seg, kv_seg, q_start, out, stream))
@@ -169,7 +178,7 @@ def index_score(q, k, w, scale, compress_rate, q_seg=None, kv_seg=None, q_start=
 def index_topk(scores, top_k, out=None, stream=None):
     """Per-row selection from scores [B,S,W] fp32 -> idx [B,S,top_k] int32."""
     B, S, W = scores.shape
-    p = Problem(B, 1, S, 1, W, 1, 1.0, int(top_k), CSA_F32)
+    p = Problem(B, 1, S, 1, W, 1, 1.0, int(top_k), CSA_F32, CSA_Q_HEAD_MAJOR)
     if out is None:
         out = torch.empty(B, S, top_k, dtype=torch.int32, device=scores.device)
     _check("csa_index_topk", index_topk_raw(p, scores, out, None, stream))
@@ -177,9 +186,9 @@ def index_topk(scores, top_k, out=None, stream=None):
 
 
 def index_fused(q, k, w, scale, compress_rate, top_k, q_seg=None, kv_seg=None, q_start=None, out=None,
-                scores_dbg=None, workspace=None, stream=None):
+                scores_dbg=None, workspace=None, stream=None, q_layout=CSA_Q_HEAD_MAJOR):
     """Scores and selection in one call -> idx [B,S,top_k] int32."""
-    p = make_problem(q, k, w, scale, compress_rate, top_k)
+    p = make_problem(q, k, w, scale, compress_rate, top_k, q_layout)
     if out is None:
         out = torch.empty(p.B, p.S, p.top_k, dtype=torch.int32, device=q.device)
     need = workspace_size(p, 1)
@@ -187,6 +196,18 @@ def index_fused(q, k, w, scale, compress_rate, top_k, q_seg=None, kv_seg=None, q
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     _check("csa_index_fused", index_fused_raw(p, q, k, w, q_seg, kv_seg, q_start, out, scores_dbg,
                                               workspace, stream))
+    return out
+
+
+def index_gather(k, idx, out=None, stream=None):
+    """Selected compressed rows: out[b,s,i,:] = k[b, idx[b,s,i], :] (zeros for -1)."""
+    B, W, D = k.shape
+    _, S, K = idx.shape
+    p = Problem(B, 1, S, D, W, 1, 1.0, int(K), CSA_BF16, CSA_Q_HEAD_MAJOR)
+    if out is None:
+        out = torch.empty(B, S, K, D, dtype=k.dtype, device=k.device)
+    _check("csa_index_gather", load().csa_index_gather(ctypes.byref(p), _ptr(k), _ptr(idx), _ptr(out),
+                                                       _stream(stream)))
     return out
 
 

@@ -16,7 +16,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libcsa_index.so")
-SOURCES = ["csa_prefill.cu", "csa_topk.cu", "csa_api.cu"]
+SOURCES = ["csa_prefill.cu", "csa_topk.cu", "csa_gather.cu", "csa_api.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -28,6 +28,7 @@ csa_status check_problem(const csa_problem* p) {
   if (p->compress_rate < 1 || p->top_k < 1) return CSA_ERR_INVALID_ARG;
   if (!(p->scale > 0.f) || !std::isfinite(p->scale)) return CSA_ERR_INVALID_ARG;
   if (p->w_dtype != CSA_BF16 && p->w_dtype != CSA_F32) return CSA_ERR_INVALID_ARG;
+  if (p->q_layout != CSA_Q_HEAD_MAJOR && p->q_layout != CSA_Q_SEQ_MAJOR) return CSA_ERR_INVALID_ARG;
   const double rows = (double)p->B * (double)p->S;
   if (rows * (double)p->W > 4.0e18 || rows * (double)p->top_k > 4.0e18) return CSA_ERR_INVALID_ARG;
   return CSA_OK;
@@ -92,15 +93,18 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// q [B,H,S,D] bf16 viewed as dims (D, H, S, B) so one box {KC, H, R, 1}
-// lands as R*H rows ordered (row j, head h) -> j*H + h.
+// q viewed as dims (D, H, S, B) so one box {KC, H, R, 1} lands as R*H rows
+// ordered (row j, head h) -> j*H + h.  Head-major [B,H,S,D] and
+// sequence-major [B,S,H,D] differ only in the strides of H and S.
 bool make_q_map(CUtensorMap* m, const csa_problem* p, const void* q, int R) {
   auto fn = encode_fn();
   if (!fn) return false;
   const int KC = (p->D % 64 == 0) ? 64 : 32;
   cuuint64_t dims[4] = {(cuuint64_t)p->D, (cuuint64_t)p->H, (cuuint64_t)p->S, (cuuint64_t)p->B};
-  cuuint64_t strides[3] = {(cuuint64_t)p->S * p->D * 2, (cuuint64_t)p->D * 2,
-                           (cuuint64_t)p->H * p->S * p->D * 2};
+  const cuuint64_t row = (cuuint64_t)p->D * 2;
+  const bool seq_major = p->q_layout == CSA_Q_SEQ_MAJOR;
+  cuuint64_t strides[3] = {seq_major ? row : (cuuint64_t)p->S * row, seq_major ? (cuuint64_t)p->H * row : row,
+                           (cuuint64_t)p->H * p->S * row};
   cuuint32_t box[4] = {(cuuint32_t)KC, (cuuint32_t)p->H, (cuuint32_t)R, 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
   const CUtensorMapSwizzle sw = (KC == 64) ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
@@ -291,12 +295,28 @@ size_t csa_index_workspace_size(const csa_problem* p, int32_t which) {
   return 0;
 }
 
+csa_status csa_index_gather(const csa_problem* p, const void* k, const int32_t* idx, void* out, void* stream) {
+  csa_status st = check_problem(p);
+  if (st != CSA_OK) return st;
+  if (k == nullptr || idx == nullptr || out == nullptr) return CSA_ERR_INVALID_ARG;
+  if (!aligned(k, 16) || !aligned(out, 16) || !aligned(idx, 4)) return CSA_ERR_INVALID_ARG;
+  if (p->D != 128 && p->D != 32) return CSA_ERR_UNSUPPORTED;
+  const int sms = num_sms();
+  if (sms <= 0) return CSA_ERR_CUDA;
+  const long long n_rows = (long long)p->B * p->S * p->top_k;
+  if (launch_gather(k, idx, out, n_rows, p->S, p->top_k, p->W, p->D, sms, static_cast<cudaStream_t>(stream)) !=
+      cudaSuccess)
+    return CSA_ERR_CUDA;
+  return CSA_OK;
+}
+
 csa_status csa_index_device_status(void* stream) {
-  uint32_t a = 0, b = 0;
+  uint32_t a = 0, b = 0, c = 0;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (take_status_prefill(&a, s) != cudaSuccess) return CSA_ERR_CUDA;
   if (take_status_other(&b, s) != cudaSuccess) return CSA_ERR_CUDA;
-  const uint32_t v = a | b;
+  if (take_status_gather(&c, s) != cudaSuccess) return CSA_ERR_CUDA;
+  const uint32_t v = a | b | c;
   if (v & kErrTimeout) return CSA_ERR_TIMEOUT;
   if (v != 0u) return CSA_ERR_DEVICE;
   return CSA_OK;
@@ -322,6 +342,6 @@ const char* csa_status_string(csa_status s) {
   return "unknown status";
 }
 
-int32_t csa_index_abi_version(void) { return 100; }
+int32_t csa_index_abi_version(void) { return 101; }
 
 }  // extern "C"

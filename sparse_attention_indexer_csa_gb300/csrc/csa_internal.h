@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <algorithm>
+
 #include "csa_score_kernel.cuh"
 
 namespace csa {
@@ -26,6 +28,11 @@ size_t index_kernel_smem(const KernelChoice& kc, int w_pad);
 cudaError_t launch_topk(const float* scores, int32_t* idx, long long rows, int W, int K,
                         cudaStream_t stream);
 int topk_threads(int W);
+
+// Gather of the selected compressed entries (D in {32, 128}).
+cudaError_t launch_gather(const void* k, const int32_t* idx, void* out, long long n_rows, int S, int K, int W, int D,
+                          int sms, cudaStream_t stream);
+cudaError_t take_status_gather(uint32_t* out, cudaStream_t stream);
 
 // Kernel that waits on a barrier nothing completes, bounded by `ns`.
 cudaError_t launch_selftest_timeout(unsigned long long ns, cudaStream_t stream);

@@ -39,14 +39,14 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_abi_version_and_strings(lib):
-    assert lib.csa_index_abi_version() == 100
+    assert lib.csa_index_abi_version() == 101
     for s in range(6):
         assert abi.status_string(s)
     assert abi.status_string(99) == "unknown status"
 
 
 def _p(**kw):
-    d = dict(B=1, H=64, S=16, D=128, W=4, compress_rate=4, scale=0.1, top_k=2, w_dtype=abi.CSA_BF16)
+    d = dict(B=1, H=64, S=16, D=128, W=4, compress_rate=4, scale=0.1, top_k=2, w_dtype=abi.CSA_BF16, q_layout=0)
     d.update(kw)
     return abi.Problem(**d)
 
@@ -62,7 +62,7 @@ def _score(lib, p, q=FAKE, k=FAKE, w=FAKE, qs=None, kvs=None, st=None, out=FAKE)
 @pytest.mark.parametrize("bad", [dict(B=0), dict(H=0), dict(S=-1), dict(D=0), dict(W=0),
                                  dict(compress_rate=0), dict(top_k=0), dict(scale=0.0),
                                  dict(scale=-1.0), dict(scale=float("inf")), dict(scale=float("nan")),
-                                 dict(w_dtype=7)])
+                                 dict(w_dtype=7), dict(q_layout=2), dict(q_layout=-1)])
 def test_bad_problem_rejected(lib, bad):
     assert _score(lib, _p(**bad)) == abi.CSA_ERR_INVALID_ARG
 

@@ -288,3 +288,16 @@ def test_decode_start_makes_all_visible():
     assert vis.all()
     vis = O.visibility(1, 1, 32768, 4, q_start=np.array([131070]))
     assert vis[0, 0, :32767].all() and not vis[0, 0, 32767]
+
+
+def test_gather_selected_matches_loops():
+    rng = np.random.default_rng(12)
+    k = rng.standard_normal((2, 9, 5))
+    idx = rng.integers(-1, 9, size=(2, 4, 3))
+    out = O.gather_selected(k, idx)
+    for b in range(2):
+        for s in range(4):
+            for i in range(3):
+                t = idx[b, s, i]
+                expect = np.zeros(5) if t < 0 else k[b, t]
+                assert np.array_equal(out[b, s, i], expect)
