@@ -379,6 +379,23 @@ def run_ours(args, wl, inp):
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
     }
+    if args.gather:  # gather of the selected rows, timed on its own over the same selection
+        gout = torch.empty(wl.B, wl.S, wl.top_k, wl.D, dtype=torch.bfloat16, device=dev)
+        for _ in range(3):
+            csa.index_gather(k, idx, out=gout, stream=stream)
+        g0 = torch.cuda.Event(enable_timing=True)
+        g1 = torch.cuda.Event(enable_timing=True)
+        n_g = 50
+        g0.record(stream)
+        for _ in range(n_g):
+            csa.index_gather(k, idx, out=gout, stream=stream)
+        g1.record(stream)
+        torch.cuda.synchronize()
+        g_ms = g0.elapsed_time(g1) / n_g
+        n_sel = int((idx >= 0).sum().item())
+        g_bytes = gout.numel() * 2 + idx.numel() * 4 + n_sel * wl.D * 2
+        line["gather"] = {"ms": g_ms, "bytes": g_bytes, "GB/s": g_bytes / (g_ms * 1e-3) / 1e9,
+                          "frac_of_hbm": g_bytes / (g_ms * 1e-3) / 1e9 / float(peaks.get("hbm_gbs", 6800.0))}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cb = oracle_sample(inp, args.cpu_seconds)
         line["cpu_baseline"] = {"value": cb["tflops"], "unit": "TFLOP/s", "cores": os.cpu_count(),
@@ -402,6 +419,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--batch", type=int, default=None, help="override B (smaller profiling case)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end measurement")
+    ap.add_argument("--gather", action="store_true",
+                    help="also time the gather of the selected compressed rows (reported, not in the step)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
