@@ -39,7 +39,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM bytes (read + write) per launch of the timed kernel, from the ncu launch
 # list summarised in profiles/ (fused_prefill_16k_launches.md).  Reset an
 # entry to None whenever that kernel changes.
-MEASURED_TRAFFIC = {"prefill_16k": 274.95e6 + 223.9e6}
+MEASURED_TRAFFIC = {"prefill_16k": None}
 
 
 # ----------------------------------------------------------------------------- work accounting

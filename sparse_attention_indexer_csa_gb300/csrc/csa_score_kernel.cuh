@@ -331,6 +331,11 @@ template <class C>
 __device__ void run_producer(const KParams& p, const Smem<C>& sm, const WaitCtl& ctl, const CUtensorMap* tq,
                              const CUtensorMap* tk) {
   uint32_t kcount = 0, qcount = 0;
+  // q blocks are read once; k tiles are re-read by every row block of the
+  // batch, except with single-row items (decode), where k streams once and
+  // should not push the scores of the selection pass out of L2
+  const uint64_t q_pol = l2_policy_evict_first();
+  const uint64_t k_pol = (C::R == 1) ? l2_policy_evict_first() : l2_policy_evict_last();
   int it = 0;
   for (int item = blockIdx.x; item < p.n_items; item += gridDim.x, ++it) {
     const int slot = it % C::SLOTS;
@@ -344,7 +349,7 @@ __device__ void run_producer(const KParams& p, const Smem<C>& sm, const WaitCtl&
       mbar_arrive_expect_tx(sm.q_full(qb), C::QBYTES);
 #pragma unroll
       for (int c = 0; c < C::NKC; ++c)
-        tma_load_4d(sm.q(qb) + c * C::QCHUNK, tq, sm.q_full(qb), c * C::KC, 0, s0, b);
+        tma_load_4d_hint(sm.q(qb) + c * C::QCHUNK, tq, sm.q_full(qb), c * C::KC, 0, s0, b, q_pol);
     }
     ++qcount;
     for (int tile = t_lo; tile < t_hi; ++tile) {
@@ -353,7 +358,7 @@ __device__ void run_producer(const KParams& p, const Smem<C>& sm, const WaitCtl&
         mbar_arrive_expect_tx(sm.k_full(st), C::KBYTES);
 #pragma unroll
         for (int c = 0; c < C::NKC; ++c)
-          tma_load_3d(sm.k(st) + c * C::KCHUNK, tk, sm.k_full(st), c * C::KC, tile * kTileT, b);
+          tma_load_3d_hint(sm.k(st) + c * C::KCHUNK, tk, sm.k_full(st), c * C::KC, tile * kTileT, b, k_pol);
       }
       ++kcount;
     }

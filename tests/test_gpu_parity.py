@@ -90,12 +90,13 @@ def _sample_rows(S, W, r, top_k, q_seg_row=None, n=1024, seed=0):
     return np.array(sorted(rows))[:max(n, len(rows))]
 
 
-@pytest.mark.parametrize("name", ["prefill_16k", "packed_8k"])
-def test_full_size_prefill(name):
+@pytest.mark.parametrize("name,seed", [("prefill_16k", 0), ("packed_8k", 0), ("packed_8k", 1)])
+def test_full_size_prefill(name, seed):
     """Fused path in the benchmarked launch configuration: selection checked on
     every row against the oracle selector on the GPU scores, and on sampled rows
-    against the oracle's own scores."""
-    wl = WORKLOADS[name]
+    against the oracle's own scores.  (packed_8k with seed 0 has no row above
+    top_k; seed 1 of the same recipe has 4030 such rows.)"""
+    wl = WORKLOADS[name].with_(seed=seed)
     inp = make_inputs(wl)
     d = to_dev(inp)
     idx_p, _ = gpu_fused(inp, d, dbg=False)
