@@ -433,23 +433,35 @@ __device__ __forceinline__ void epilogue_accumulate(uint32_t t_row, const float*
 #pragma unroll
   for (int jj = 0; jj < RW; ++jj) acc[jj] = 0.f;
   if constexpr (H == 64) {
-    // one 64-column TMEM load per row (all heads of the row); four
-    // independent packed-FMA chains
+    // 2*RW chunks of 32 columns (row jj, heads hh*32 .. hh*32+31); the load
+    // of the next chunk is in flight while the current one is reduced with
+    // four independent packed-FMA chains
+    float va[32], vb[32];
+    float2 a[4];
+    tmem_ld32_start(t_row + (uint32_t)(hf * RW * H), va);
+    tmem_wait32(va);
 #pragma unroll
-    for (int jj = 0; jj < RW; ++jj) {
-      const int j = hf * RW + jj;
-      float v[64];
-      tmem_ld64(t_row + (uint32_t)(j * H), v);
-      const float2* w2 = reinterpret_cast<const float2*>(ws + j * H);
-      float2 a[4];
+    for (int c = 0; c < 2 * RW; ++c) {
+      float(&cur)[32] = (c & 1) ? vb : va;
+      float(&nxt)[32] = (c & 1) ? va : vb;
+      if (c + 1 < 2 * RW) tmem_ld32_start(t_row + (uint32_t)(hf * RW * H + (c + 1) * 32), nxt);
+      const int jj = c >> 1, hh = c & 1;
+      const float4* w4 = reinterpret_cast<const float4*>(ws + (hf * RW + jj) * H + hh * 32);
+      if (hh == 0) {
 #pragma unroll
-      for (int q = 0; q < 4; ++q) a[q] = make_float2(0.f, 0.f);
-#pragma unroll
-      for (int i = 0; i < H / 2; ++i) {
-        const float2 r2 = make_float2(fmaxf(v[2 * i], 0.f), fmaxf(v[2 * i + 1], 0.f));
-        a[i & 3] = ffma2(w2[i], r2, a[i & 3]);
+        for (int q = 0; q < 4; ++q) a[q] = make_float2(0.f, 0.f);
       }
-      acc[jj] = ((a[0].x + a[0].y) + (a[1].x + a[1].y)) + ((a[2].x + a[2].y) + (a[3].x + a[3].y));
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float4 wq = w4[i];
+        const float2 r0 = make_float2(fmaxf(cur[4 * i], 0.f), fmaxf(cur[4 * i + 1], 0.f));
+        const float2 r1 = make_float2(fmaxf(cur[4 * i + 2], 0.f), fmaxf(cur[4 * i + 3], 0.f));
+        a[(2 * i) & 3] = ffma2(make_float2(wq.x, wq.y), r0, a[(2 * i) & 3]);
+        a[(2 * i + 1) & 3] = ffma2(make_float2(wq.z, wq.w), r1, a[(2 * i + 1) & 3]);
+      }
+      if (hh == 1)
+        acc[jj] = ((a[0].x + a[0].y) + (a[1].x + a[1].y)) + ((a[2].x + a[2].y) + (a[3].x + a[3].y));
+      if (c + 1 < 2 * RW) tmem_wait32(nxt);
     }
   } else {
     static_assert((C::RW * H) % 8 == 0, "small-head path loads 8 columns at a time");

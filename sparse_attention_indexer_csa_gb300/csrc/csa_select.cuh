@@ -298,9 +298,12 @@ __device__ void team_topk_row(float* row, int t0, int n, uint32_t K, const RowSt
   auto bin_of = [&](float x) -> uint32_t {  // in [0, NB-1] for any finite x
     return __float_as_uint(fmaxf(fminf(fmaf(x, scale, bias), nb1), 0.0f) + 8388608.0f) - 0x4B000000u;
   };
-  const float4* row4 = reinterpret_cast<const float4*>(row + t0);
+  // shared-space addresses: entry e of the row's range at row_s + 4*e
+  const uint32_t row_s = smem_u32(row + t0);
+  const uint32_t hist_s = smem_u32(bs->hist), keep_s = smem_u32(bs->keep);
+  const uint32_t cand_s = smem_u32(bs->cand), cand_t_s = smem_u32(bs->cand_t);
+  const uint32_t ncand_s = smem_u32(&bs->bcast[3]), seg_sel_s = smem_u32(bs->seg_sel);
   const int n4 = n >> 2;
-  const float4 ninf4 = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
 #pragma unroll
   for (int j = 0; j < PER; ++j) bs->hist[team.tid * PER + j] = 0u;
   if (team.tid < 32) {
@@ -308,19 +311,28 @@ __device__ void team_topk_row(float* row, int t0, int n, uint32_t K, const RowSt
     bs->seg_sel[team.tid] = 0u;
   }
   team.sync();
-  // 1. histogram, four float4 loads in flight per thread
+  // 1. histogram: four float4 loads in flight per thread, then sixteen
+  //    predicated shared-memory adds with no returned value
 #pragma unroll 1
   for (int i0 = (int)team.tid; i0 < n4; i0 += 4 * NT) {
     float4 a[4];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) a[q] = (i0 + q * NT < n4) ? row4[i0 + q * NT] : ninf4;
+    for (int q = 0; q < 4; ++q)
+      a[q] = (i0 + q * NT < n4) ? lds_f4(row_s + 16u * (uint32_t)(i0 + q * NT))
+                                : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+    uint32_t addr[16];
+    bool vis[16];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       const float xs[4] = {a[q].x, a[q].y, a[q].z, a[q].w};
 #pragma unroll
-      for (int u = 0; u < 4; ++u)
-        if (xs[u] > -INFINITY) atomicAdd(&bs->hist[bin_of(xs[u])], 1u);
+      for (int u = 0; u < 4; ++u) {
+        vis[4 * q + u] = xs[u] > -INFINITY;
+        addr[4 * q + u] = hist_s + 4u * bin_of(xs[u]);
+      }
     }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) red_add_shared_if(addr[i], 1u, vis[i]);
   }
   team.sync();
   // 2. b*: thread t owns bins [t*PER, (t+1)*PER); suffix sums over threads
@@ -364,39 +376,62 @@ __device__ void team_topk_row(float* row, int t0, int n, uint32_t K, const RowSt
     return;
   }
   const uint32_t need = K - above;
-  // 3. bitmap of sure entries, per-segment counts, gather b*; two chunks in flight
+  const uint32_t lt_mask = (1u << lane) - 1u;
+  // 3. bitmap of sure entries and per-segment counts from ballots; members
+  //    of b* gathered by a ballot compaction (one slot reservation per warp
+  //    and pair of chunks); two chunks in flight
   const int seg_chunks = (chunks + NW - 1) / NW;
   const int c_lo = min(chunks, (int)warp * seg_chunks);
   const int c_hi = min(chunks, c_lo + seg_chunks);
-  uint32_t gt = 0;
+  uint32_t gt = 0;  // warp-uniform
 #pragma unroll 1
   for (int c0 = c_lo; c0 < c_hi; c0 += 2) {
     float4 v[2];
 #pragma unroll
-    for (int q = 0; q < 2; ++q) v[q] = (c0 + q < c_hi) ? row4[(c0 + q) * 32 + (int)lane] : ninf4;
+    for (int q = 0; q < 2; ++q)
+      v[q] = (c0 + q < c_hi) ? lds_f4(row_s + 16u * (uint32_t)((c0 + q) * 32 + (int)lane))
+                             : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+    uint32_t sure[8], memb[8];
+    float xk[8];
 #pragma unroll
     for (int q = 0; q < 2; ++q) {
-      const int c = c0 + q;
       const float xs[4] = {v[q].x, v[q].y, v[q].z, v[q].w};
-      uint32_t bal[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const bool vis = xs[u] > -INFINITY;
-        const uint32_t b = vis ? bin_of(xs[u]) : 0u;
-        const bool sure = vis && b > bstar;
-        bal[u] = __ballot_sync(0xFFFFFFFFu, sure);
-        gt += sure;
-        if (vis && b == bstar) {
-          const uint32_t slot = atomicAdd(&bs->bcast[3], 1u);
-          bs->cand[slot] = score_key(xs[u]);
-          bs->cand_t[slot] = (uint32_t)(c * 128 + 4 * (int)lane + u);  // relative to t0
-        }
+        const uint32_t bb = bin_of(xs[u]);
+        xk[4 * q + u] = xs[u];
+        sure[4 * q + u] = __ballot_sync(0xFFFFFFFFu, vis && bb > bstar);
+        memb[4 * q + u] = __ballot_sync(0xFFFFFFFFu, vis && bb == bstar);
       }
-      if (lane == 0 && c < c_hi)
-        *reinterpret_cast<uint4*>(&bs->keep[4 * c]) = make_uint4(bal[0], bal[1], bal[2], bal[3]);
+    }
+    if (lane == 0) {
+      sts_u4(keep_s + 16u * (uint32_t)c0, make_uint4(sure[0], sure[1], sure[2], sure[3]));
+      if (c0 + 1 < c_hi) sts_u4(keep_s + 16u * (uint32_t)(c0 + 1), make_uint4(sure[4], sure[5], sure[6], sure[7]));
+    }
+    uint32_t nm = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      gt += __popc(sure[i]);
+      nm += __popc(memb[i]);
+    }
+    if (nm != 0u) {  // warp-uniform
+      uint32_t slot = 0;
+      if (lane == 0) slot = atom_add_shared(ncand_s, nm);
+      slot = __shfl_sync(0xFFFFFFFFu, slot, 0);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        if ((memb[i] >> lane) & 1u) {
+          const uint32_t o = slot + __popc(memb[i] & lt_mask);
+          if (o < (uint32_t)CAP) {
+            sts_u32(cand_s + 4u * o, score_key(xk[i]));
+            sts_u32(cand_t_s + 4u * o, (uint32_t)((c0 + i / 4) * 128 + 4 * (int)lane + (i & 3)));  // relative to t0
+          }
+        }
+        slot += __popc(memb[i]);
+      }
     }
   }
-  gt = __reduce_add_sync(0xFFFFFFFFu, gt);
   if (lane == 0) bs->seg_gt[warp] = gt;
   team.sync();
   // 4. exact rank inside b*
@@ -411,34 +446,31 @@ __device__ void team_topk_row(float* row, int t0, int n, uint32_t K, const RowSt
     }
     if (rank < need) {
       const uint32_t c = ti >> 7, l = (ti >> 2) & 31u, u = ti & 3u;
-      atomicOr(&bs->keep[4 * c + u], 1u << l);
-      atomicAdd(&bs->seg_sel[c / (uint32_t)seg_chunks], 1u);
+      red_or_shared(keep_s + 4u * (4u * c + u), 1u << l);
+      red_add_shared_if(seg_sel_s + 4u * (c / (uint32_t)seg_chunks), 1u, true);
     }
   }
   team.sync();
-  // 5. ordered write from the bitmap
+  // 5. ordered write from the bitmap: positions from popcounts, predicated stores
   uint32_t base = 0, total = 0;
   for (int w = 0; w < NW; ++w) {
     const uint32_t cnt = bs->seg_gt[w] + bs->seg_sel[w];
     base += (w < (int)warp) ? cnt : 0u;
     total += cnt;
   }
-  const uint32_t lt_mask = (1u << lane) - 1u;
-#pragma unroll 2
+#pragma unroll 4
   for (int c = c_lo; c < c_hi; ++c) {
-    const uint4 mw = *reinterpret_cast<const uint4*>(&bs->keep[4 * c]);
-    const uint32_t ms[4] = {mw.x, mw.y, mw.z, mw.w};
-    uint32_t pos = base;
-#pragma unroll
-    for (int u = 0; u < 4; ++u) pos += __popc(ms[u] & lt_mask);
+    const uint4 mw = lds_u4(keep_s + 16u * (uint32_t)c);
+    const uint32_t b0 = (mw.x >> lane) & 1u, b1 = (mw.y >> lane) & 1u, b2 = (mw.z >> lane) & 1u;
+    const uint32_t b3 = (mw.w >> lane) & 1u;
+    const uint32_t p0 = base + __popc(mw.x & lt_mask) + __popc(mw.y & lt_mask) + __popc(mw.z & lt_mask) +
+                        __popc(mw.w & lt_mask);
+    const uint32_t p1 = p0 + b0, p2 = p1 + b1, p3 = p2 + b2;
     const int tb = t0 + c * 128 + 4 * (int)lane;
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      if ((ms[u] >> lane) & 1u) {
-        if (pos < K) out[pos] = tb + u;
-        ++pos;
-      }
-    }
+    if (b0 && p0 < K) out[p0] = tb;
+    if (b1 && p1 < K) out[p1] = tb + 1;
+    if (b2 && p2 < K) out[p2] = tb + 2;
+    if (b3 && p3 < K) out[p3] = tb + 3;
     base += __popc(mw.x) + __popc(mw.y) + __popc(mw.z) + __popc(mw.w);
   }
   for (uint32_t i = min(total, K) + team.tid; i < K; i += NT) out[i] = -1;
