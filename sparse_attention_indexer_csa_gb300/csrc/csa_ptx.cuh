@@ -328,6 +328,24 @@ __device__ __forceinline__ void sts_u4(uint32_t a, uint4 v) {
   asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
                : "memory");
 }
+// predicated forms: the store happens only where `pred` holds, without a branch
+__device__ __forceinline__ void sts_u4_if(uint32_t a, uint4 v, bool pred) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.u32 p, %5, 0;\n\t"
+      "@p st.shared.v4.u32 [%0], {%1, %2, %3, %4};\n\t}" ::"r"(a),
+      "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"((uint32_t)pred)
+      : "memory");
+}
+__device__ __forceinline__ void sts_u32x2_if(uint32_t a0, uint32_t v0, uint32_t a1, uint32_t v1, bool pred) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.u32 p, %4, 0;\n\t"
+      "@p st.shared.u32 [%0], %1;\n\t"
+      "@p st.shared.u32 [%2], %3;\n\t}" ::"r"(a0),
+      "r"(v0), "r"(a1), "r"(v1), "r"((uint32_t)pred)
+      : "memory");
+}
 __device__ __forceinline__ void sts_u32(uint32_t a, uint32_t v) {
   asm volatile("st.shared.u32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
 }

@@ -378,12 +378,14 @@ __device__ void team_topk_row(float* row, int t0, int n, uint32_t K, const RowSt
   const uint32_t need = K - above;
   const uint32_t lt_mask = (1u << lane) - 1u;
   // 3. bitmap of sure entries and per-segment counts from ballots; members
-  //    of b* gathered by a ballot compaction (one slot reservation per warp
-  //    and pair of chunks); two chunks in flight
+  //    of b* gathered by a ballot compaction (slots from a register count in
+  //    one-warp teams, else one reservation per warp and pair of chunks);
+  //    two chunks in flight, stores predicated rather than branched
   const int seg_chunks = (chunks + NW - 1) / NW;
   const int c_lo = min(chunks, (int)warp * seg_chunks);
   const int c_hi = min(chunks, c_lo + seg_chunks);
-  uint32_t gt = 0;  // warp-uniform
+  uint32_t gt = 0;      // warp-uniform
+  uint32_t ncand = 0u;  // one-warp teams: members gathered so far
 #pragma unroll 1
   for (int c0 = c_lo; c0 < c_hi; c0 += 2) {
     float4 v[2];
@@ -405,30 +407,43 @@ __device__ void team_topk_row(float* row, int t0, int n, uint32_t K, const RowSt
         memb[4 * q + u] = __ballot_sync(0xFFFFFFFFu, vis && bb == bstar);
       }
     }
-    if (lane == 0) {
-      sts_u4(keep_s + 16u * (uint32_t)c0, make_uint4(sure[0], sure[1], sure[2], sure[3]));
-      if (c0 + 1 < c_hi) sts_u4(keep_s + 16u * (uint32_t)(c0 + 1), make_uint4(sure[4], sure[5], sure[6], sure[7]));
-    }
-    uint32_t nm = 0;
+    sts_u4_if(keep_s + 16u * (uint32_t)c0, make_uint4(sure[0], sure[1], sure[2], sure[3]), lane == 0);
+    sts_u4_if(keep_s + 16u * (uint32_t)(c0 + 1), make_uint4(sure[4], sure[5], sure[6], sure[7]),
+              lane == 0 && c0 + 1 < c_hi);
+    // counts as balanced sums (short dependency chains)
+    uint32_t pm[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      gt += __popc(sure[i]);
-      nm += __popc(memb[i]);
-    }
-    if (nm != 0u) {  // warp-uniform
-      uint32_t slot = 0;
-      if (lane == 0) slot = atom_add_shared(ncand_s, nm);
-      slot = __shfl_sync(0xFFFFFFFFu, slot, 0);
+    for (int i = 0; i < 8; ++i) pm[i] = __popc(memb[i]);
+    gt += ((__popc(sure[0]) + __popc(sure[1])) + (__popc(sure[2]) + __popc(sure[3]))) +
+          ((__popc(sure[4]) + __popc(sure[5])) + (__popc(sure[6]) + __popc(sure[7])));
+    // exclusive prefix of the member counts over the eight ballots
+    uint32_t pre[8];
+    pre[0] = 0u;
+    pre[1] = pm[0];
+    pre[2] = pm[0] + pm[1];
+    pre[3] = pre[2] + pm[2];
+    const uint32_t h4 = pre[2] + (pm[2] + pm[3]);
+    pre[4] = h4;
+    pre[5] = h4 + pm[4];
+    pre[6] = h4 + (pm[4] + pm[5]);
+    pre[7] = pre[6] + pm[6];
+    const uint32_t nm = pre[7] + pm[7];
+    if (nm != 0u) {  // warp-uniform: most pairs of chunks hold no member
+      uint32_t slot;
+      if constexpr (NT == 32) {  // one warp: the running member count lives in a register
+        slot = ncand;
+        ncand += nm;
+      } else {
+        slot = 0;
+        if (lane == 0) slot = atom_add_shared(ncand_s, nm);
+        slot = __shfl_sync(0xFFFFFFFFu, slot, 0);
+      }
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        if ((memb[i] >> lane) & 1u) {
-          const uint32_t o = slot + __popc(memb[i] & lt_mask);
-          if (o < (uint32_t)CAP) {
-            sts_u32(cand_s + 4u * o, score_key(xk[i]));
-            sts_u32(cand_t_s + 4u * o, (uint32_t)((c0 + i / 4) * 128 + 4 * (int)lane + (i & 3)));  // relative to t0
-          }
-        }
-        slot += __popc(memb[i]);
+        const uint32_t o = slot + pre[i] + __popc(memb[i] & lt_mask);
+        sts_u32x2_if(cand_s + 4u * o, score_key(xk[i]), cand_t_s + 4u * o,
+                     (uint32_t)((c0 + i / 4) * 128 + 4 * (int)lane + (i & 3)),  // entry relative to t0
+                     ((memb[i] >> lane) & 1u) && o < (uint32_t)CAP);
       }
     }
   }
