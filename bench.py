@@ -36,10 +36,12 @@ from csa_inputs import WORKLOADS, Inputs, make_inputs  # noqa: E402
 
 METRIC = "indexer useful TFLOP/s and query rows/s at S=16K; % of bf16 tensor peak"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-# DRAM bytes (read + write) per launch of the timed kernel, from the ncu launch
-# list summarised in profiles/ (fused_prefill_16k_launches.md).  Reset an
-# entry to None whenever that kernel changes.
-MEASURED_TRAFFIC = {"prefill_16k": None}
+# DRAM bytes (read + write) per timed unit, from the ncu launch lists
+# summarised in profiles/: prefill_16k per launch of the fused kernel
+# (fused_prefill_16k_launches.md); decode_32k per step, i.e. the score launch
+# plus the selection launch, the same span the decode roofline is timed over
+# (decode_32k_launches.md).  Reset an entry to None whenever a kernel changes.
+MEASURED_TRAFFIC = {"prefill_16k": 498.2e6, "decode_32k": 550.8e6}
 
 
 # ----------------------------------------------------------------------------- work accounting
