@@ -264,6 +264,11 @@ __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32
       : "memory");
 }
 
+// Global store with an L2 eviction-priority policy (from l2_policy_*).
+__device__ __forceinline__ void st_global_hint(float* addr, float v, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(addr), "f"(v), "l"(pol) : "memory");
+}
+
 // Orders this thread's earlier generic-proxy global accesses with later
 // async-proxy (bulk copy) accesses.
 __device__ __forceinline__ void fence_proxy_async_global() {

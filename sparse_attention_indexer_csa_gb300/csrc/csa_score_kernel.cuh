@@ -514,6 +514,7 @@ __device__ void run_epilogue(const KParams& p, const Smem<C>& sm, const WaitCtl&
   const bool segs = p.q_seg != nullptr;
   const uint32_t t_lane = tmem_base + ((uint32_t)(quarter * 32) << 16);
   uint32_t acount = 0, nt = 0;
+  const uint64_t sc_pol = l2_policy_evict_last();
   int it = 0;
   for (int item = blockIdx.x; item < p.n_items; item += gridDim.x, ++it) {
     const int slot = it % C::SLOTS;
@@ -578,7 +579,13 @@ __device__ void run_epilogue(const KParams& p, const Smem<C>& sm, const WaitCtl&
             scnt[jj] += 1u;
           }
         }
-        if (p.scores != nullptr && s < p.S && t < p.W) p.scores[((size_t)b * p.S + s) * p.W + t] = val;
+        if (p.scores != nullptr && s < p.S && t < p.W) {
+          float* dst = p.scores + ((size_t)b * p.S + s) * p.W + t;
+          if constexpr (C::R == 1)  // single-row items (decode): the selection pass re-reads them from L2
+            st_global_hint(dst, val, sc_pol);
+          else
+            *dst = val;
+        }
       }
     }
     if constexpr (C::FUSED) {  // row statistics, then hand the slot to the select warps

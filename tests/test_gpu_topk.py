@@ -1,6 +1,7 @@
 """GPU selection kernel on crafted score matrices, checked exactly against the
-oracle selector.  The cases drive every branch of the selection: continuous
-scores (binned search), heavy ties (threshold bin over capacity: radix
+oracle selector.  The cases drive every branch of the selection, in the
+one-CTA kernel and, for rows longer than 16384, the four-CTA cluster kernel:
+continuous scores (binned search), heavy ties (threshold bin over capacity: radix
 search), all-equal rows, signed zeros, a value range whose width overflows
 fp32, denormals, scores far from zero relative to their spread, masked
 entries, and rows with fewer visible entries than k."""
@@ -54,7 +55,10 @@ def _case(kind, rows, W, rng):
 KINDS = ["normal", "ties", "few_values", "equal", "zeros", "huge", "denormal", "offset", "relu_like"]
 
 
-@pytest.mark.parametrize("W,k", [(1000, 300), (4096, 2048), (300, 1), (32768, 2048), (257, 400), (9000, 700)])
+# W > 16384 runs on clusters of four CTAs per row: an odd W (scalar staging,
+# ragged last segment), the longest row, top_k above one CTA's segment, k = 1
+@pytest.mark.parametrize("W,k", [(1000, 300), (4096, 2048), (300, 1), (32768, 2048), (257, 400), (9000, 700),
+                                 (20001, 3000), (49152, 4096), (16385, 9000), (32768, 1)])
 @pytest.mark.parametrize("kind", KINDS)
 def test_topk_kernel_matches_oracle_selector(kind, W, k):
     rng = np.random.default_rng(abs(hash((kind, W, k))) % 2**32)
