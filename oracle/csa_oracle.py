@@ -31,8 +31,19 @@ values):
   stable sort, not a selection algorithm.
 * ``brute_force_scores`` -- the same definition written as plain Python loops
   over (b, s, t, h, d), for tiny shapes only.
+* ``index_scores_vjp`` -- the backward of the score step: for a cotangent
+  ``g[B,S,W]`` of the scores, the gradients ``dq, dk, dw`` of
+  ``sum(g * score)`` over the visible entries ("Add StreamIndex Kernel for CSA
+  [Deepseek v4]", Description: the custom_vjp whose backward is the
+  autodiff of the reference computation).  Readings: masked entries are
+  constants (``-inf``) and take no gradient, so ``g`` is used only where
+  visible; the ReLU derivative at 0 is 0.
 
-Parity pins (see ``tests/test_oracle.py``): a hand-worked 2-head / 4-entry
+Parity pins (see ``tests/test_oracle.py``): for the backward, central finite
+differences on tiny shapes, Euler's identity for the degree-1 positive
+homogeneity of the score in q, in k and in w separately (each of
+``sum(q*dq)``, ``sum(k*dk)``, ``sum(w*dw)`` equals ``sum(g*score)``),
+linearity in g and independence of g at masked entries.  For the forward: a hand-worked 2-head / 4-entry
 example, brute force on tiny shapes, the H=1 / w=1 / scale=1 special case
 reducing to ``max(Q K^T, 0)`` and ``argsort``, and invariants (masked entries
 never selected, w=0 gives zero scores and the lowest visible indices,
@@ -195,3 +206,37 @@ def brute_force_scores(q, k, w, scale, compress_rate, q_start=None, q_seg=None, 
                     acc += float(Wt[b, s, h]) * (x if x > 0.0 else 0.0)
                 out[b][s][t] = acc
     return np.array(out, dtype=np.float64)
+
+
+def index_scores_vjp(q, k, w, scale: float, compress_rate: int, g,
+                     q_start=None, q_seg=None, kv_seg=None):
+    """float64 ``(dq [B,H,S,D], dk [B,W,D], dw [B,S,H])`` for the cotangent
+    ``g [B,S,W]`` of the visible scores.
+
+    With ``x = q[b,h,s,:] . k[b,t,:]`` and ``gm = g`` on visible entries, 0
+    elsewhere (chain rule through ``score = sum_h w * ReLU(scale * x)``):
+
+        dw[b,s,h] = sum_t gm[b,s,t] * ReLU(scale * x)
+        dx        = gm[b,s,t] * w[b,s,h] * scale * [scale * x > 0]
+        dq[b,h]   = dx @ k[b]          dk[b] = sum_h dx^T @ q[b,h]
+
+    one library matmul per contraction, per batch and head.
+    """
+    Q, K, Wt, G = _f64(q), _f64(k), _f64(w), _f64(g)
+    B, H, S, D = Q.shape
+    W = K.shape[1]
+    c = scale_value(scale)
+    vis = visibility(B, S, W, compress_rate, q_start, q_seg, kv_seg)
+    gm = np.where(vis, G, 0.0)
+    dq = np.zeros_like(Q)
+    dk = np.zeros_like(K)
+    dw = np.zeros((B, S, H), dtype=np.float64)
+    for b in range(B):
+        for h in range(H):
+            x = Q[b, h] @ K[b].T                                # [S, W]
+            cx = c * x
+            dw[b, :, h] = (gm[b] * np.maximum(cx, 0.0)).sum(axis=1)
+            dx = gm[b] * Wt[b, :, h][:, None] * c * (cx > 0.0)
+            dq[b, h] = dx @ K[b]
+            dk[b] += dx.T @ Q[b, h]
+    return dq, dk, dw

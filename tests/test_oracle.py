@@ -301,3 +301,80 @@ def test_gather_selected_matches_loops():
                 t = idx[b, s, i]
                 expect = np.zeros(5) if t < 0 else k[b, t]
                 assert np.array_equal(out[b, s, i], expect)
+
+
+# --------------------------------------------------------------------------- backward
+def test_backward_hand_example():
+    g, q, k, w, _ = _hand()
+    ex = g["backward_example"]
+    G = np.zeros((1, g["S"], g["W"]))
+    for s_, t_, v in ex["g_entries"]:
+        G[0, s_, t_] = v
+    dq, dk, dw = O.index_scores_vjp(q, k, w, g["scale"], g["compress_rate"], G)
+    edq, edk, edw = np.zeros_like(dq), np.zeros_like(dk), np.zeros_like(dw)
+    for h, s_, d, v in ex["expected_dq_nonzero"]:
+        edq[0, h, s_, d] = v
+    for t_, d, v in ex["expected_dk_nonzero"]:
+        edk[0, t_, d] = v
+    for s_, h, v in ex["expected_dw_nonzero"]:
+        edw[0, s_, h] = v
+    assert np.array_equal(dq, edq) and np.array_equal(dk, edk) and np.array_equal(dw, edw)
+
+
+def _loss(q, k, w, scale, r, G, q_start=None, q_seg=None, kv_seg=None):
+    sc = O.index_scores(q, k, w, scale, r, q_start, q_seg, kv_seg)
+    return float(np.where(np.isfinite(sc), G * np.where(np.isfinite(sc), sc, 0.0), 0.0).sum())
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_backward_finite_differences(seed):
+    rng = np.random.default_rng(300 + seed)
+    B, H, S, D, W, r = 1, 2, 6, 3, 4, 2
+    segs = seed == 1
+    start = [3] if seed == 2 else None
+    q, k, w, q_start, q_seg, kv_seg = _rand_problem(rng, B, H, S, D, W, r, segs, start)
+    G = rng.standard_normal((B, S, W))
+    scale = 0.61
+    c = O.scale_value(scale)
+    x = np.einsum("bhsd,btd->bhst", q, k)
+    assert np.min(np.abs(c * x)) > 1e-3  # away from the ReLU kink
+    dq, dk, dw = O.index_scores_vjp(q, k, w, scale, r, G, q_start, q_seg, kv_seg)
+    eps = 1e-6
+    for arr, grad in ((q, dq), (k, dk), (w, dw)):
+        for i in np.ndindex(arr.shape):
+            old = arr[i]
+            arr[i] = old + eps
+            lp = _loss(q, k, w, scale, r, G, q_start, q_seg, kv_seg)
+            arr[i] = old - eps
+            lm = _loss(q, k, w, scale, r, G, q_start, q_seg, kv_seg)
+            arr[i] = old
+            assert abs((lp - lm) / (2 * eps) - grad[i]) < 1e-6 * (1 + abs(grad[i])), (i, grad[i])
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_backward_euler_homogeneity(seed):
+    # score is positively homogeneous of degree 1 in q, in k and in w, so
+    # sum(q*dq) = sum(k*dk) = sum(w*dw) = sum(g*score) over visible entries
+    rng = np.random.default_rng(400 + seed)
+    q, k, w, q_start, q_seg, kv_seg = _rand_problem(rng, 2, 3, 20, 8, 9, 2, seed == 1, [5, 0] if seed == 2 else None)
+    G = rng.standard_normal((2, 20, 9))
+    dq, dk, dw = O.index_scores_vjp(q, k, w, 0.3, 2, G, q_start, q_seg, kv_seg)
+    L = _loss(q, k, w, 0.3, 2, G, q_start, q_seg, kv_seg)
+    for a, d in ((q, dq), (k, dk), (w, dw)):
+        assert abs(float((a * d).sum()) - L) < 1e-10 * (1 + abs(L))
+
+
+def test_backward_linear_in_g_and_blind_to_masked_g():
+    rng = np.random.default_rng(7)
+    q, k, w, q_start, q_seg, kv_seg = _rand_problem(rng, 1, 2, 16, 4, 8, 2, True, None)
+    G1, G2 = rng.standard_normal((2, 1, 16, 8))
+    a = O.index_scores_vjp(q, k, w, 0.5, 2, G1 + 2.0 * G2, q_start, q_seg, kv_seg)
+    b1 = O.index_scores_vjp(q, k, w, 0.5, 2, G1, q_start, q_seg, kv_seg)
+    b2 = O.index_scores_vjp(q, k, w, 0.5, 2, G2, q_start, q_seg, kv_seg)
+    for x, y, z in zip(a, b1, b2):
+        np.testing.assert_allclose(x, y + 2.0 * z, rtol=1e-12, atol=1e-12)
+    vis = O.visibility(1, 16, 8, 2, q_start, q_seg, kv_seg)
+    G3 = np.where(vis, G1, 1e6)  # anything at masked entries
+    c = O.index_scores_vjp(q, k, w, 0.5, 2, G3, q_start, q_seg, kv_seg)
+    for x, y in zip(c, b1):
+        assert np.array_equal(x, y)
