@@ -410,6 +410,76 @@ def run_ours(args, wl, inp):
         dist.destroy_process_group()
 
 
+def run_backward(args, wl, inp):
+    """One line for the backward of the score step (csa_index_backward):
+    dq, dk, dw for a fixed seeded cotangent of the scores; per step the
+    chunked P kernel, the chunk copies of q and the cuBLAS GEMMs."""
+    import sparse_attention_indexer_csa_gb300 as csa
+
+    if not torch.cuda.is_available():
+        raise RuntimeError("bench.py needs a CUDA GPU for the library arm")
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    csa.load()
+    stream = torch.cuda.current_stream(dev)
+    wk = work(inp)
+    q, k, w = inp.q.to(dev), inp.k.to(dev), inp.w.to(dev)
+    q_seg = None if inp.q_seg is None else inp.q_seg.to(dev)
+    kv_seg = None if inp.kv_seg is None else inp.kv_seg.to(dev)
+    q_start = None if inp.q_start is None else inp.q_start.to(dev)
+    gen = torch.Generator().manual_seed(wl.seed + 1000)
+    g = torch.randn(wl.B, wl.S, wl.W, generator=gen, dtype=torch.float32).to(dev)
+    p = csa.make_problem(q, k, w, wl.scale, wl.compress_rate, 1)
+    dq = torch.empty(wl.B, wl.H, wl.S, wl.D, dtype=torch.float32, device=dev)
+    dk = torch.empty(wl.B, wl.W, wl.D, dtype=torch.float32, device=dev)
+    dw = torch.empty(wl.B, wl.S, wl.H, dtype=torch.float32, device=dev)
+    ws = torch.empty(csa.workspace_size(p, 2), dtype=torch.uint8, device=dev)
+
+    def step():
+        st = csa.abi.index_backward_raw(p, q, k, w, q_seg, kv_seg, q_start, g, dq, dk, dw, ws, stream)
+        if st != csa.CSA_OK:
+            raise RuntimeError(f"csa_index_backward returned {st}")
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if csa.device_status(stream) != csa.CSA_OK:
+        raise RuntimeError("device status word reports an error after warm-up")
+    clocks = ClockSampler(0)
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.25)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms = e0.elapsed_time(e1) / args.steps
+    if csa.device_status(stream) != csa.CSA_OK:
+        raise RuntimeError("device status word reports an error after the timed region")
+    # useful work: the logits recomputed, dq and dk, 2*H*D flops each per visible pair
+    flops = 3.0 * wk["flops"]
+    peaks, peak_src = read_peaks()
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    achieved = flops / (ms * 1e-3) / 1e12
+    line = {
+        "metric": "indexer backward useful TFLOP/s (dq, dk, dw of the visible scores)", "value": achieved,
+        "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "mode": "backward", "config": config_dict(wl, 1),
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": None,
+                     "peak_source": f"{peak_src} ({'MEASURED_PEAKS.json' if peak_src == 'measured' else 'recipe fallback'})",
+                     "achieved_counts": "3 x 2*H*D per visible pair (logits recomputed, dq, dk); the whole step, "
+                                        "several kernels and library GEMMs"},
+        "e2e": None, "gpu_launches": None, "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -421,6 +491,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--batch", type=int, default=None, help="override B (smaller profiling case)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end measurement")
+    ap.add_argument("--backward", action="store_true",
+                    help="time the backward of the score step instead (its own JSON line)")
     ap.add_argument("--gather", action="store_true",
                     help="also time the gather of the selected compressed rows (reported, not in the step)")
     args = ap.parse_args()
@@ -437,6 +509,9 @@ def main():
         run_reference(args, wl, inp)
         return
     inp = make_inputs(wl.with_(seed=wl.seed + rank))
+    if args.backward:
+        run_backward(args, wl, inp)
+        return
     run_ours(args, wl, inp)
 
 

@@ -152,9 +152,35 @@ csa_status csa_index_fused_noalloc(const csa_problem* p, const void* q, const vo
                                    const int32_t* q_seg, const int32_t* kv_seg, const int64_t* q_start,
                                    int32_t* idx, void* stream);
 
+/* Backward of the score step: the gradients of sum(g * score) over the
+ * visible entries, for a cotangent g of the scores ("Add StreamIndex Kernel
+ * for CSA [Deepseek v4]", Description: the custom_vjp whose backward is the
+ * autodiff of the reference computation).  With x = q[b,h,s,:].k[b,t,:] and
+ * gm = g on visible entries, 0 on masked ones (masked scores are constants):
+ *   dw[b,s,h] = sum_t gm * ReLU(scale * x)
+ *   P         = gm * w[b,s,h] * scale * [x > 0]
+ *   dq[b,h,s,:] = sum_t P * k[b,t,:],   dk[b,t,:] = sum_{h,s} P * q[b,h,s,:].
+ * Inputs as for csa_index_score (q head-major only); g [B,S,W] fp32 (values
+ * at masked entries are ignored); writes dq [B,H,S,D], dk [B,W,D] and
+ * dw [B,S,H], all fp32, every element.  Needs `workspace`:
+ * csa_index_workspace_size(p, 2) bytes (256-byte aligned), which holds P for
+ * one chunk of up to 1024 query rows ([H, rows, W] bf16) and a copy of the
+ * chunk's q rows: the [B,H,S,W] tensor is never formed.  Per chunk: a
+ * tensor-core kernel forms P and dw, then two library GEMMs (cuBLAS, fp32
+ * accumulation) form dq and add the chunk's share of dk.  P is rounded to
+ * bf16 before the GEMMs; dw is accumulated in fp32 from fp32 products.
+ * Several kernels and GEMMs run on `stream` per chunk; the call returns once
+ * they are enqueued.  Supported: H = 64, D = 128, CSA_Q_HEAD_MAJOR.
+ * Added in ABI version 102.                                              */
+csa_status csa_index_backward(const csa_problem* p, const void* q, const void* k, const void* w,
+                              const int32_t* q_seg, const int32_t* kv_seg, const int64_t* q_start,
+                              const float* g, float* dq, float* dk, float* dw, void* workspace,
+                              size_t workspace_bytes, void* stream);
+
 /* Bytes of device workspace an entry point needs: which = 0 for
- * csa_index_topk (always 0), 1 for csa_index_fused.  Depends only on the
- * problem (no device query).  Returns 0 when the problem is invalid.      */
+ * csa_index_topk (always 0), 1 for csa_index_fused, 2 for
+ * csa_index_backward.  Depends only on the problem (no device query).
+ * Returns 0 when the problem is invalid.                                  */
 size_t csa_index_workspace_size(const csa_problem* p, int32_t which);
 
 /* Synchronises `stream`, then reads and clears the device status word of

@@ -26,6 +26,7 @@ EXPORTED = (
     "csa_index_fused",
     "csa_index_fused_noalloc",
     "csa_index_gather",
+    "csa_index_backward",
     "csa_index_workspace_size",
     "csa_index_device_status",
     "csa_index_selftest_timeout",
@@ -70,6 +71,7 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.csa_index_fused.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     lib.csa_index_fused_noalloc.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp]
     lib.csa_index_gather.argtypes = [P, vp, vp, vp, vp]
+    lib.csa_index_backward.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     lib.csa_index_workspace_size.argtypes = [P, i32]
     lib.csa_index_workspace_size.restype = sz
     lib.csa_index_device_status.argtypes = [vp]
@@ -78,6 +80,7 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.csa_status_string.restype = ctypes.c_char_p
     lib.csa_index_abi_version.restype = i32
     for name in ("csa_index_score", "csa_index_topk", "csa_index_fused", "csa_index_fused_noalloc", "csa_index_gather",
+                 "csa_index_backward",
                  "csa_index_device_status",
                  "csa_index_selftest_timeout"):
         getattr(lib, name).restype = i32
@@ -152,6 +155,14 @@ def index_fused_noalloc_raw(p: Problem, q, k, w, q_seg, kv_seg, q_start, idx, st
                                           _ptr(q_start), _ptr(idx), _stream(stream))
 
 
+def index_backward_raw(p: Problem, q, k, w, q_seg, kv_seg, q_start, g, dq, dk, dw, workspace=None,
+                       stream=None) -> int:
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    return load().csa_index_backward(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(w), _ptr(q_seg), _ptr(kv_seg),
+                                     _ptr(q_start), _ptr(g), _ptr(dq), _ptr(dk), _ptr(dw), _ptr(workspace), nbytes,
+                                     _stream(stream))
+
+
 def workspace_size(p: Problem, which: int) -> int:
     return int(load().csa_index_workspace_size(ctypes.byref(p), which))
 
@@ -197,6 +208,21 @@ def index_fused(q, k, w, scale, compress_rate, top_k, q_seg=None, kv_seg=None, q
     _check("csa_index_fused", index_fused_raw(p, q, k, w, q_seg, kv_seg, q_start, out, scores_dbg,
                                               workspace, stream))
     return out
+
+
+def index_backward(q, k, w, scale, compress_rate, g, q_seg=None, kv_seg=None, q_start=None, workspace=None,
+                   stream=None):
+    """Gradients of sum(g * score) over the visible scores -> (dq [B,H,S,D],
+    dk [B,W,D], dw [B,S,H]), fp32, for g [B,S,W] fp32."""
+    p = make_problem(q, k, w, scale, compress_rate, 1, CSA_Q_HEAD_MAJOR)
+    dq = torch.empty(p.B, p.H, p.S, p.D, dtype=torch.float32, device=q.device)
+    dk = torch.empty(p.B, p.W, p.D, dtype=torch.float32, device=q.device)
+    dw = torch.empty(p.B, p.S, p.H, dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = torch.empty(workspace_size(p, 2), dtype=torch.uint8, device=q.device)
+    _check("csa_index_backward", index_backward_raw(p, q, k, w, q_seg, kv_seg, q_start, g, dq, dk, dw,
+                                                    workspace, stream))
+    return dq, dk, dw
 
 
 def index_gather(k, idx, out=None, stream=None):

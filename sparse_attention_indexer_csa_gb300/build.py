@@ -2,7 +2,8 @@
 
 Each translation unit under ``csrc/`` is compiled by nvcc in parallel and the
 objects are linked into one shared library with the CUDA runtime linked
-statically, so the library only needs the NVIDIA driver at run time.
+statically; at run time it needs the NVIDIA driver and the toolkit's cuBLAS
+(the backward's two GEMMs), located through the library's rpath.
 """
 from __future__ import annotations
 
@@ -16,7 +17,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libcsa_index.so")
-SOURCES = ["csa_prefill.cu", "csa_topk.cu", "csa_gather.cu", "csa_api.cu"]
+SOURCES = ["csa_prefill.cu", "csa_topk.cu", "csa_gather.cu", "csa_backward.cu", "csa_api.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -25,6 +26,15 @@ def nvcc() -> str:
     if not os.path.exists(cand):
         raise RuntimeError("nvcc not found: the CUDA toolkit is required to build libcsa_index.so")
     return cand
+
+
+def cuda_lib_dir(cc: str) -> str:
+    """Library directory of the toolkit that owns `cc` (for cuBLAS)."""
+    root = os.path.dirname(os.path.dirname(os.path.realpath(cc)))
+    for cand in (os.path.join(root, "lib64"), os.path.join(root, "lib")):
+        if os.path.exists(os.path.join(cand, "libcublas.so")):
+            return cand
+    return os.path.join(root, "lib64")
 
 
 def _flags(extra):
@@ -57,7 +67,10 @@ def build(verbose: bool = False, extra_flags=()) -> str:
         msg = "\n".join(f"--- {s}\n{t}" for s, t in failed)
         raise RuntimeError(f"nvcc failed:\n{msg}")
     tmp = LIB + ".tmp"
-    link = [cc] + ARCH + ["-shared", "-o", tmp] + objs + ["-cudart", "static"]
+    libdir = cuda_lib_dir(cc)
+    # the backward's dq / dk GEMMs use cuBLAS, found at run time through the rpath
+    link = [cc] + ARCH + ["-shared", "-o", tmp] + objs + ["-cudart", "static", "-L", libdir, "-lcublas",
+                                                       "-Xlinker", "-rpath", "-Xlinker", libdir]
     res = subprocess.run(link, stdout=subprocess.PIPE, stderr=subprocess.STDOUT)
     if res.returncode != 0:
         raise RuntimeError("link failed:\n" + res.stdout.decode(errors="replace"))

@@ -128,6 +128,36 @@ bool make_k_map(CUtensorMap* m, const csa_problem* p, const void* k) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Chunk buffer of the backward: P [H, rows, w_pad] bf16 as dims (w_pad, rows, H);
+// box {64, 2, 64} = 64 entries of one pair of rows for every head, stored
+// from a 128-byte-swizzled staging tile.
+bool make_p_map(CUtensorMap* m, const void* pbuf, int rows, int w_pad, int H) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)w_pad, (cuuint64_t)rows, (cuuint64_t)H};
+  cuuint64_t strides[2] = {(cuuint64_t)w_pad * 2, (cuuint64_t)rows * w_pad * 2};
+  cuuint32_t box[3] = {64, 2, (cuuint32_t)H};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(pbuf), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+constexpr int kBwdChunkRows = 1024;  // query rows per backward chunk
+
+int bwd_chunk_rows(const csa_problem* p) {
+  const int rc = std::min(p->S, kBwdChunkRows);
+  return (rc + 1) & ~1;
+}
+size_t round256(size_t x) { return (x + 255) & ~(size_t)255; }
+size_t bwd_p_bytes(const csa_problem* p) {
+  return round256((size_t)p->H * bwd_chunk_rows(p) * w_pad_of(p) * 2);
+}
+size_t backward_workspace_bytes(const csa_problem* p) {
+  if (check_problem(p) != CSA_OK) return 0;
+  return bwd_p_bytes(p) + round256((size_t)p->H * bwd_chunk_rows(p) * p->D * 2);
+}
+
 csa_status run_index_kernel(const csa_problem* p, bool fused, const void* q, const void* k, const void* w,
                             const int32_t* q_seg, const int32_t* kv_seg, const int64_t* q_start, float* scores,
                             int32_t* idx, float* ring, cudaStream_t stream) {
@@ -292,7 +322,91 @@ csa_status csa_index_fused_noalloc(const csa_problem* p, const void* q, const vo
 
 size_t csa_index_workspace_size(const csa_problem* p, int32_t which) {
   if (which == 1) return fused_workspace_bytes(p);
+  if (which == 2) return backward_workspace_bytes(p);
   return 0;
+}
+
+csa_status csa_index_backward(const csa_problem* p, const void* q, const void* k, const void* w,
+                              const int32_t* q_seg, const int32_t* kv_seg, const int64_t* q_start, const float* g,
+                              float* dq, float* dk, float* dw, void* workspace, size_t workspace_bytes,
+                              void* stream) {
+  csa_status st = check_problem(p);
+  if (st != CSA_OK) return st;
+  if ((st = check_inputs(p, q, k, w, q_seg, kv_seg, q_start)) != CSA_OK) return st;
+  if (g == nullptr || dq == nullptr || dk == nullptr || dw == nullptr) return CSA_ERR_INVALID_ARG;
+  if (!aligned(g, 4) || !aligned(dq, 4) || !aligned(dk, 4) || !aligned(dw, 4)) return CSA_ERR_INVALID_ARG;
+  if (p->H != 64 || p->D != 128 || p->q_layout != CSA_Q_HEAD_MAJOR) return CSA_ERR_UNSUPPORTED;
+  const size_t need = backward_workspace_bytes(p);
+  if (workspace == nullptr || workspace_bytes < need || !aligned(workspace, 256)) return CSA_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int rc = bwd_chunk_rows(p), w_pad = w_pad_of(p);
+  uint8_t* pbuf = static_cast<uint8_t*>(workspace);
+  uint8_t* qcbuf = pbuf + bwd_p_bytes(p);
+  CUtensorMap tq, tk;
+  if (!make_q_map(&tq, p, q, 2) || !make_k_map(&tk, p, k)) return CSA_ERR_CUDA;
+  // dk accumulates over chunks; dq rows and dw are written once each
+  if (cudaMemsetAsync(dk, 0, (size_t)p->B * p->W * p->D * sizeof(float), s) != cudaSuccess) return CSA_ERR_CUDA;
+  const size_t qrow = (size_t)p->D * 2;  // bytes of one q row
+  for (int b = 0; b < p->B; ++b) {
+    for (int s0 = 0; s0 < p->S; s0 += rc) {
+      const int rows = std::min(rc, p->S - s0);
+      // GEMM range: entries below the chunk's largest visible threshold (the
+      // last row's), or all entries when a per-sequence offset is given (its
+      // value lives on the device)
+      const int w_eff = q_start ? p->W : std::min<long long>(p->W, ((long long)s0 + rows) / p->compress_rate);
+      float* dq_chunk = dq + ((size_t)b * p->H * p->S + s0) * p->D;
+      float* dw_chunk = dw + ((size_t)b * p->S + s0) * p->H;
+      if (w_eff == 0) {  // no visible entry in the chunk
+        if (cudaMemset2DAsync(dq_chunk, (size_t)p->S * p->D * sizeof(float), 0, (size_t)rows * p->D * sizeof(float),
+                              p->H, s) != cudaSuccess ||
+            cudaMemsetAsync(dw_chunk, 0, (size_t)rows * p->H * sizeof(float), s) != cudaSuccess)
+          return CSA_ERR_CUDA;
+        continue;
+      }
+      CUtensorMap tp;
+      if (!make_p_map(&tp, pbuf, rows, w_pad, p->H)) return CSA_ERR_CUDA;
+      BwdParams bp;
+      std::memset(&bp, 0, sizeof(bp));
+      bp.B = p->B;
+      bp.S = p->S;
+      bp.W = p->W;
+      bp.r = p->compress_rate;
+      bp.b = b;
+      bp.s_base = s0;
+      bp.rows = rows;
+      bp.n_items = (rows + 1) / 2;
+      bp.T_eff = (w_eff + kTileT - 1) / kTileT;
+      bp.w_f32 = (p->w_dtype == CSA_F32) ? 1 : 0;
+      bp.scale = p->scale;
+      bp.w = w;
+      bp.q_seg = q_seg;
+      bp.kv_seg = kv_seg;
+      bp.q_start = q_start;
+      bp.g = g;
+      bp.dw = dw;
+      bp.wait_ns = kWaitNs;
+      if (launch_backward_kernel(tq, tk, tp, bp, s) != cudaSuccess) return CSA_ERR_CUDA;
+      // the chunk's q rows, head by head, into one [H, rows, D] block
+      const uint8_t* qsrc = static_cast<const uint8_t*>(q) + ((size_t)b * p->H * p->S + s0) * qrow;
+      if (cudaMemcpy2DAsync(qcbuf, (size_t)rows * qrow, qsrc, (size_t)p->S * qrow, (size_t)rows * qrow, p->H,
+                            cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+        return CSA_ERR_CUDA;
+      BwdGemms gm;
+      gm.H = p->H;
+      gm.D = p->D;
+      gm.rows = rows;
+      gm.w_eff = w_eff;
+      gm.w_pad = w_pad;
+      gm.p = pbuf;
+      gm.k = static_cast<const uint8_t*>(k) + (size_t)b * p->W * qrow;
+      gm.qc = qcbuf;
+      gm.dq = dq_chunk;
+      gm.dq_head_stride = (long long)p->S * p->D;
+      gm.dk = dk + (size_t)b * p->W * p->D;
+      if (!backward_gemms(gm, s)) return CSA_ERR_CUDA;
+    }
+  }
+  return CSA_OK;
 }
 
 csa_status csa_index_gather(const csa_problem* p, const void* k, const int32_t* idx, void* out, void* stream) {
@@ -311,12 +425,13 @@ csa_status csa_index_gather(const csa_problem* p, const void* k, const int32_t* 
 }
 
 csa_status csa_index_device_status(void* stream) {
-  uint32_t a = 0, b = 0, c = 0;
+  uint32_t a = 0, b = 0, c = 0, d = 0;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (take_status_prefill(&a, s) != cudaSuccess) return CSA_ERR_CUDA;
   if (take_status_other(&b, s) != cudaSuccess) return CSA_ERR_CUDA;
   if (take_status_gather(&c, s) != cudaSuccess) return CSA_ERR_CUDA;
-  const uint32_t v = a | b | c;
+  if (take_status_backward(&d, s) != cudaSuccess) return CSA_ERR_CUDA;
+  const uint32_t v = a | b | c | d;
   if (v & kErrTimeout) return CSA_ERR_TIMEOUT;
   if (v != 0u) return CSA_ERR_DEVICE;
   return CSA_OK;
@@ -342,6 +457,6 @@ const char* csa_status_string(csa_status s) {
   return "unknown status";
 }
 
-int32_t csa_index_abi_version(void) { return 101; }
+int32_t csa_index_abi_version(void) { return 102; }
 
 }  // extern "C"

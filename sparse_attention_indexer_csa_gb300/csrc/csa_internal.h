@@ -34,6 +34,40 @@ cudaError_t launch_gather(const void* k, const int32_t* idx, void* out, long lon
                           int sms, cudaStream_t stream);
 cudaError_t take_status_gather(uint32_t* out, cudaStream_t stream);
 
+// Backward of the score step for one batch and one chunk of query rows
+// (csa_backward.cu): P in bf16 into the chunk buffer and dw, then two GEMMs.
+struct BwdParams {
+  int B, S, W, r;
+  int b;        // batch of this launch
+  int s_base;   // first row of the chunk
+  int rows;     // rows in the chunk
+  int n_items;  // pairs of rows: (rows + 1) / 2
+  int T_eff;    // tiles of the chunk's GEMM range: P is written for [0, T_eff*128)
+  int w_f32;
+  float scale;
+  const void* w;
+  const int32_t* q_seg;
+  const int32_t* kv_seg;
+  const int64_t* q_start;
+  const float* g;
+  float* dw;
+  unsigned long long wait_ns;
+};
+struct BwdGemms {
+  int H, D, rows, w_eff, w_pad;
+  const void* p;       // [H, rows, w_pad] bf16
+  const void* k;       // [W, D] bf16 of the batch
+  const void* qc;      // [H, rows, D] bf16 copy of the chunk's q rows
+  float* dq;           // dq[b, 0, s_base, 0]; heads dq_head_stride floats apart
+  long long dq_head_stride;
+  float* dk;           // dk[b] [W, D]
+};
+cudaError_t launch_backward_kernel(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tp,
+                                   const BwdParams& bp, cudaStream_t stream);
+size_t backward_kernel_smem();
+bool backward_gemms(const BwdGemms& gm, cudaStream_t stream);
+cudaError_t take_status_backward(uint32_t* out, cudaStream_t stream);
+
 // Kernel that waits on a barrier nothing completes, bounded by `ns`.
 cudaError_t launch_selftest_timeout(unsigned long long ns, cudaStream_t stream);
 

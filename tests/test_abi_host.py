@@ -39,7 +39,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_abi_version_and_strings(lib):
-    assert lib.csa_index_abi_version() == 101
+    assert lib.csa_index_abi_version() == 102
     for s in range(6):
         assert abi.status_string(s)
     assert abi.status_string(99) == "unknown status"
@@ -109,3 +109,29 @@ def test_selftest_argument_checks(lib):
 def test_binding_fails_loudly_without_library(tmp_path):
     with pytest.raises(RuntimeError):
         abi.load(str(tmp_path / "missing.so"))
+
+
+def _bwd(lib, p, g=FAKE, dq=FAKE, dk=FAKE, dw=FAKE, ws=FAKE, nbytes=1 << 40, q=FAKE):
+    return lib.csa_index_backward(ctypes.byref(p), q, FAKE, FAKE, None, None, None, g, dq, dk, dw, ws, nbytes, None)
+
+
+def test_backward_workspace_size():
+    # P of one chunk of rows ([H, rows, W_pad] bf16) + the chunk's q rows ([H, rows, D] bf16)
+    assert abi.workspace_size(_p(S=16, W=4), 2) == 64 * 16 * 128 * 2 + 64 * 16 * 128 * 2
+    assert abi.workspace_size(_p(S=16384, W=4096), 2) == 64 * 1024 * 4096 * 2 + 64 * 1024 * 128 * 2
+    assert abi.workspace_size(_p(S=5, W=300), 2) == 64 * 6 * 384 * 2 + 64 * 6 * 128 * 2  # rows rounded to pairs
+    assert abi.workspace_size(_p(B=0), 2) == 0
+
+
+def test_backward_argument_checks(lib):
+    assert _bwd(lib, _p(B=0)) == abi.CSA_ERR_INVALID_ARG
+    for kw in (dict(g=None), dict(dq=None), dict(dk=None), dict(dw=None), dict(q=None), dict(dq=ODD)):
+        assert _bwd(lib, _p(), **kw) == abi.CSA_ERR_INVALID_ARG, kw
+    # workspace missing, short or misaligned
+    need = abi.workspace_size(_p(), 2)
+    assert _bwd(lib, _p(), ws=None) == abi.CSA_ERR_INVALID_ARG
+    assert _bwd(lib, _p(), nbytes=need - 1) == abi.CSA_ERR_INVALID_ARG
+    assert _bwd(lib, _p(), ws=ctypes.c_void_p(0x10010)) == abi.CSA_ERR_INVALID_ARG
+    # only H=64, D=128, head-major q
+    assert _bwd(lib, _p(H=4, D=32)) == abi.CSA_ERR_UNSUPPORTED
+    assert _bwd(lib, _p(q_layout=1)) == abi.CSA_ERR_UNSUPPORTED
