@@ -129,14 +129,14 @@ bool make_k_map(CUtensorMap* m, const csa_problem* p, const void* k) {
 }
 
 // Chunk buffer of the backward: P [H, rows, w_pad] bf16 as dims (w_pad, rows, H);
-// box {64, 2, 64} = 64 entries of one pair of rows for every head, stored
-// from a 128-byte-swizzled staging tile.
+// box {64, 1, 32} = 64 entries of one row for 32 heads, stored from one
+// epilogue warp's 128-byte-swizzled staging tile.
 bool make_p_map(CUtensorMap* m, const void* pbuf, int rows, int w_pad, int H) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[3] = {(cuuint64_t)w_pad, (cuuint64_t)rows, (cuuint64_t)H};
   cuuint64_t strides[2] = {(cuuint64_t)w_pad * 2, (cuuint64_t)rows * w_pad * 2};
-  cuuint32_t box[3] = {64, 2, (cuuint32_t)H};
+  cuuint32_t box[3] = {64, 1, 32};
   cuuint32_t estr[3] = {1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(pbuf), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -375,6 +375,8 @@ csa_status csa_index_backward(const csa_problem* p, const void* q, const void* k
       bp.s_base = s0;
       bp.rows = rows;
       bp.n_items = (rows + 1) / 2;
+      bp.grid = num_sms();
+      if (bp.grid <= 0) return CSA_ERR_CUDA;
       bp.T_eff = (w_eff + kTileT - 1) / kTileT;
       bp.w_f32 = (p->w_dtype == CSA_F32) ? 1 : 0;
       bp.scale = p->scale;

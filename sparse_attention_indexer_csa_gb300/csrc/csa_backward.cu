@@ -13,17 +13,22 @@
 // workspace -- never the whole [B,H,S,W]) and dw in registers; dq and dk are
 // then two plain GEMMs over that chunk (cuBLAS).
 //
-// Kernel layout (one CTA per pair of query rows, 192 threads):
-//   warp 0  TMA: the q block (2 rows x 64 heads x 128, as the UMMA A operand:
-//           M = 128 rows (row j, head h) -> 64 j + h) once, then k tiles
-//           (128 entries, the B operand, N = 128) into three stages;
+// Kernel layout (persistent: each CTA takes pairs of query rows in turn, 320
+// threads):
+//   warp 0  TMA: per pair the q block (2 rows x 64 heads x 128, as the UMMA A
+//           operand: M = 128 rows (row j, head h) -> 64 j + h), then its k
+//           tiles (128 entries, the B operand, N = 128) into three stages;
 //   warp 1  TMEM owner and UMMA issuer: per k tile one 128x128x128 product
 //           into one of two 128-column accumulators;
-//   warps 2-5  epilogue: warp w reads TMEM lanes 32*(w%4) .. (rows (j, h)),
-//           so each thread owns one (row, head) and walks the tile's 128
-//           entries: dw in a register, P converted to bf16 into a
-//           128-byte-swizzled staging tile that one thread writes out with
-//           3-D TMA stores (box {64 entries, 2 rows, 64 heads}).
+//   warps 2-9  epilogue: warp w reads TMEM lanes 32*(w%4) .. (rows (j, h))
+//           and one half of the tile's 128 entries (warps 2-5 the first,
+//           6-9 the second), so each thread owns one (row, head) and walks
+//           64 entries per tile: dw in a register (the halves added once per
+//           pair), P converted to bf16 into the warp's own 128-byte-swizzled
+//           staging tile (32 heads x 64 entries), which lane 0 writes out
+//           with a 3-D TMA store (box {64 entries, 1 row, 32 heads}); each
+//           warp double-buffers its staging, so the warps never wait for
+//           one another inside a tile.
 // Tiles past the pair's visible range but inside the chunk's GEMM range are
 // written as zeros without any product.
 #include <cublas_v2.h>
@@ -45,18 +50,19 @@ constexpr uint32_t kBQBytes = kBQChunk * kBNKC;     // 32 KB
 constexpr uint32_t kBKChunk = kTileT * 128;         // 16 KB
 constexpr uint32_t kBKBytes = kBKChunk * kBNKC;     // 32 KB
 constexpr int kBStages = 3;
-constexpr uint32_t kBPHalf = kBM * 128;             // 16 KB: 128 rows x 64 entries of bf16
-constexpr uint32_t kBPTile = 2 * kBPHalf;           // 32 KB
+constexpr uint32_t kBPWarp = 32 * 128;              // 4 KB: one warp's 32 heads x 64 entries of bf16
 constexpr uint32_t kBIdesc = idesc_bf16_f32(kBM, kTileT);
-constexpr int kBThreads = 192;
+constexpr int kBEpiWarps = 8;
+constexpr int kBThreads = 64 + 32 * kBEpiWarps;
 constexpr uint32_t kBTmemCols = 256;                // two 128-column accumulators
 constexpr uint32_t kBEpiBar = 2;                    // named barrier of the epilogue warps
 
 constexpr uint32_t OFF_BQ = 0;
 constexpr uint32_t OFF_BK = OFF_BQ + kBQBytes;
 constexpr uint32_t OFF_BP = OFF_BK + kBStages * kBKBytes;
-constexpr uint32_t OFF_BG = OFF_BP + 2 * kBPTile;          // 4 warps x 128 fp32 cotangents
-constexpr uint32_t OFF_BBAR = OFF_BG + 4 * kTileT * 4;     // 1 + 2*stages + 4 barriers
+constexpr uint32_t OFF_BG = OFF_BP + kBEpiWarps * 2 * kBPWarp;  // 8 warps x 64 fp32 cotangents
+constexpr uint32_t OFF_BDW = OFF_BG + kBEpiWarps * 64 * 4;       // 2 x 128 partial dw of the second half
+constexpr uint32_t OFF_BBAR = OFF_BDW + 2 * kBM * 4;             // 2 + 2*stages + 4 barriers
 constexpr uint32_t OFF_BMISC = OFF_BBAR + 16 * 8;
 constexpr uint32_t kBSmem = OFF_BMISC + 64 + 1024;         // + alignment slack
 
@@ -64,14 +70,16 @@ struct BSm {
   uint8_t* base;
   __device__ uint8_t* q() const { return base + OFF_BQ; }
   __device__ uint8_t* k(int i) const { return base + OFF_BK + i * kBKBytes; }
-  __device__ uint8_t* ptile(int i) const { return base + OFF_BP + i * kBPTile; }
-  __device__ float* g(int e) const { return reinterpret_cast<float*>(base + OFF_BG) + e * kTileT; }
+  __device__ uint8_t* pstage(int e, int i) const { return base + OFF_BP + (e * 2 + i) * kBPWarp; }
+  __device__ float* g(int e) const { return reinterpret_cast<float*>(base + OFF_BG) + e * 64; }
+  __device__ float* dwp(int i) const { return reinterpret_cast<float*>(base + OFF_BDW) + i * kBM; }
   __device__ uint64_t* bar(int i) const { return reinterpret_cast<uint64_t*>(base + OFF_BBAR) + i; }
   __device__ uint64_t* q_full() const { return bar(0); }
-  __device__ uint64_t* k_full(int i) const { return bar(1 + i); }
-  __device__ uint64_t* k_empty(int i) const { return bar(1 + kBStages + i); }
-  __device__ uint64_t* acc_full(int i) const { return bar(1 + 2 * kBStages + i); }
-  __device__ uint64_t* acc_empty(int i) const { return bar(3 + 2 * kBStages + i); }
+  __device__ uint64_t* q_empty() const { return bar(1); }
+  __device__ uint64_t* k_full(int i) const { return bar(2 + i); }
+  __device__ uint64_t* k_empty(int i) const { return bar(2 + kBStages + i); }
+  __device__ uint64_t* acc_full(int i) const { return bar(2 + 2 * kBStages + i); }
+  __device__ uint64_t* acc_empty(int i) const { return bar(4 + 2 * kBStages + i); }
   __device__ uint32_t* tmem_slot() const { return reinterpret_cast<uint32_t*>(base + OFF_BMISC); }
   __device__ volatile uint32_t* abort_flag() const {
     return reinterpret_cast<volatile uint32_t*>(base + OFF_BMISC + 4);
@@ -87,6 +95,21 @@ __device__ __forceinline__ int row_threshold(const BwdParams& p, int s) {
   return (int)tv;
 }
 
+// Pair number `pair` of the chunk: its first row (relative and absolute), the
+// visible thresholds of its two rows and the tiles that need products.
+struct PairInfo {
+  int sl0, s0, thr0, thr1, t_hi;
+};
+__device__ __forceinline__ PairInfo pair_info(const BwdParams& p, int pair) {
+  PairInfo pi;
+  pi.sl0 = 2 * pair;
+  pi.s0 = p.s_base + pi.sl0;
+  pi.thr0 = row_threshold(p, pi.s0);
+  pi.thr1 = (pi.sl0 + 1 < p.rows) ? row_threshold(p, pi.s0 + 1) : 0;
+  pi.t_hi = min(p.T_eff, (max(pi.thr0, pi.thr1) + kTileT - 1) / kTileT);
+  return pi;
+}
+
 __global__ void __launch_bounds__(kBThreads, 1)
     csa_backward_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                         const __grid_constant__ CUtensorMap tmap_p, const BwdParams p) {
@@ -95,23 +118,17 @@ __global__ void __launch_bounds__(kBThreads, 1)
   const BSm sm{base};
   const int warp = threadIdx.x / 32;
   const uint32_t lane = lane_id();
-  // pairs in reverse order: the longest rows (most tiles) start first
-  const int pair = p.n_items - 1 - (int)blockIdx.x;
-  const int sl0 = 2 * pair;         // first row of the pair, relative to the chunk
-  const int s0 = p.s_base + sl0;    // absolute row
-  const int thr0 = row_threshold(p, s0);
-  const int thr1 = (sl0 + 1 < p.rows) ? row_threshold(p, s0 + 1) : 0;
-  const int t_hi = min(p.T_eff, (max(thr0, thr1) + kTileT - 1) / kTileT);  // tiles with products
 
   if (threadIdx.x == 0) {
     mbar_init(sm.q_full(), 1);
+    mbar_init(sm.q_empty(), 1);
     for (int i = 0; i < kBStages; ++i) {
       mbar_init(sm.k_full(i), 1);
       mbar_init(sm.k_empty(i), 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(sm.acc_full(i), 1);
-      mbar_init(sm.acc_empty(i), 4);
+      mbar_init(sm.acc_empty(i), kBEpiWarps);
     }
     *sm.abort_flag() = 0u;
     fence_mbar_init();
@@ -130,152 +147,194 @@ __global__ void __launch_bounds__(kBThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *sm.tmem_slot();
   const WaitCtl ctl{sm.abort_flag(), p.wait_ns};
+  // pairs in reverse order (the longest rows, most tiles, first), strided over the CTAs
 
   if (warp == 0) {
-    if (lane == 0 && t_hi > 0) {
+    if (lane == 0) {
       const uint64_t q_pol = l2_policy_evict_first(), k_pol = l2_policy_evict_last();
-      mbar_arrive_expect_tx(sm.q_full(), kBQBytes);
-#pragma unroll
-      for (int c = 0; c < kBNKC; ++c)
-        tma_load_4d_hint(sm.q() + c * kBQChunk, &tmap_q, sm.q_full(), c * 64, 0, s0, p.b, q_pol);
-      for (int tile = 0; tile < t_hi; ++tile) {
-        const int st = tile % kBStages;
-        if (!mbar_wait(sm.k_empty(st), ((tile / kBStages) & 1) ^ 1, ctl)) break;
-        mbar_arrive_expect_tx(sm.k_full(st), kBKBytes);
+      uint32_t qcount = 0, kcount = 0;
+      for (int it = blockIdx.x; it < p.n_items; it += gridDim.x) {
+        const PairInfo pi = pair_info(p, p.n_items - 1 - it);
+        if (pi.t_hi == 0) continue;
+        if (!mbar_wait(sm.q_empty(), (qcount & 1u) ^ 1u, ctl)) break;
+        mbar_arrive_expect_tx(sm.q_full(), kBQBytes);
 #pragma unroll
         for (int c = 0; c < kBNKC; ++c)
-          tma_load_3d_hint(sm.k(st) + c * kBKChunk, &tmap_k, sm.k_full(st), c * 64, tile * kTileT, p.b, k_pol);
+          tma_load_4d_hint(sm.q() + c * kBQChunk, &tmap_q, sm.q_full(), c * 64, 0, pi.s0, p.b, q_pol);
+        ++qcount;
+        bool ok = true;
+        for (int tile = 0; tile < pi.t_hi; ++tile, ++kcount) {
+          const int st = kcount % kBStages;
+          if (!(ok = mbar_wait(sm.k_empty(st), ((kcount / kBStages) & 1u) ^ 1u, ctl))) break;
+          mbar_arrive_expect_tx(sm.k_full(st), kBKBytes);
+#pragma unroll
+          for (int c = 0; c < kBNKC; ++c)
+            tma_load_3d_hint(sm.k(st) + c * kBKChunk, &tmap_k, sm.k_full(st), c * 64, tile * kTileT, p.b, k_pol);
+        }
+        if (!ok) break;
       }
+      // no copy may still be landing in shared memory when the CTA exits
+      volatile uint32_t dummy = 0;
+      const WaitCtl drain_ctl{&dummy, ctl.limit_ns};
+      for (uint32_t i = 0; i < (uint32_t)kBStages && i < kcount; ++i) {
+        const uint32_t last = kcount - 1 - i;
+        mbar_wait(sm.k_full(last % kBStages), (last / kBStages) & 1u, drain_ctl);
+      }
+      if (qcount > 0) mbar_wait(sm.q_full(), (qcount - 1) & 1u, drain_ctl);
     }
   } else if (warp == 1) {
-    if (lane == 0 && t_hi > 0) {
-      const bool q_ok = mbar_wait(sm.q_full(), 0, ctl);
-      tc_fence_after();
+    if (lane == 0) {
+      uint32_t qcount = 0, kcount = 0, acount = 0;
       const uint32_t q_addr = smem_u32(sm.q());
-      for (int tile = 0; tile < t_hi; ++tile) {
-        const int st = tile % kBStages, a = tile & 1;
-        const bool k_ok = mbar_wait(sm.k_full(st), (tile / kBStages) & 1, ctl);
-        const bool a_ok = mbar_wait(sm.acc_empty(a), ((tile >> 1) & 1) ^ 1, ctl);
+      for (int it = blockIdx.x; it < p.n_items; it += gridDim.x) {
+        const PairInfo pi = pair_info(p, p.n_items - 1 - it);
+        if (pi.t_hi == 0) continue;
+        const bool q_ok = mbar_wait(sm.q_full(), qcount & 1u, ctl);
         tc_fence_after();
-        if (q_ok && k_ok && a_ok) {
-          const uint32_t k_addr = smem_u32(sm.k(st));
-          const uint32_t d_tmem = tmem_base + (uint32_t)(a * kTileT);
+        bool ok = q_ok;
+        for (int tile = 0; tile < pi.t_hi; ++tile, ++kcount, ++acount) {
+          const int st = kcount % kBStages, a = acount & 1;
+          const bool k_ok = ok && mbar_wait(sm.k_full(st), (kcount / kBStages) & 1u, ctl);
+          const bool a_ok = k_ok && mbar_wait(sm.acc_empty(a), ((acount >> 1) & 1u) ^ 1u, ctl);
+          tc_fence_after();
+          ok = q_ok && k_ok && a_ok;
+          if (ok) {
+            const uint32_t k_addr = smem_u32(sm.k(st));
+            const uint32_t d_tmem = tmem_base + (uint32_t)(a * kTileT);
 #pragma unroll
-          for (int c = 0; c < kBNKC; ++c) {
+            for (int c = 0; c < kBNKC; ++c) {
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t adesc = smem_desc_kmajor(q_addr + c * kBQChunk + kk * 32, 128);
-              const uint64_t bdesc = smem_desc_kmajor(k_addr + c * kBKChunk + kk * 32, 128);
-              umma_bf16(d_tmem, adesc, bdesc, kBIdesc, (c | kk) != 0 ? 1u : 0u);
+              for (int kk = 0; kk < 4; ++kk) {
+                const uint64_t adesc = smem_desc_kmajor(q_addr + c * kBQChunk + kk * 32, 128);
+                const uint64_t bdesc = smem_desc_kmajor(k_addr + c * kBKChunk + kk * 32, 128);
+                umma_bf16(d_tmem, adesc, bdesc, kBIdesc, (c | kk) != 0 ? 1u : 0u);
+              }
             }
           }
+          umma_commit(sm.k_empty(st));
+          umma_commit(sm.acc_full(a));
+          if (!ok) break;
         }
-        umma_commit(sm.k_empty(st));
-        umma_commit(sm.acc_full(a));
-        if (!(q_ok && k_ok && a_ok)) break;
+        umma_commit(sm.q_empty());  // the q block may be replaced once these products are done
+        ++qcount;
+        if (!ok) break;
       }
     }
   } else {
-    // epilogue: thread = TMEM lane m = 32*quarter + lane = (row j, head h)
+    // epilogue: thread = TMEM lane m = 32*quarter + lane = (row j, head h);
+    // warp half hf takes entries hf*64 .. hf*64+63 of every tile
     const int e = warp - 2;
+    const int hf = e >> 2;
     const int quarter = warp & 3;
     const int m = quarter * 32 + (int)lane;
     const int j = m >> 6, h = m & 63;  // row of the pair (warp-uniform), head
-    const int s = s0 + j;
-    const bool row_ok = (sl0 + j < p.rows) && s < p.S;
-    const int thr = j ? thr1 : thr0;
+    const int h0 = 32 * (quarter & 1);  // first head of this warp
     const bool segs = p.q_seg != nullptr;
-    const int seg = (segs && row_ok) ? p.q_seg[(size_t)p.b * p.S + s] : 0;
-    float wc = 0.f;
-    if (row_ok) {
-      const size_t off = ((size_t)p.b * p.S + s) * kBH + h;
-      wc = (p.w_f32 ? reinterpret_cast<const float*>(p.w)[off]
-                    : __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p.w)[off])) *
-           p.scale;
-    }
     const uint32_t t_lane = tmem_base + ((uint32_t)(quarter * 32) << 16);
     float* gb = sm.g(e);
-    // staging row of this thread in the TMA box order {entry, row, head}
-    const uint32_t srow = (uint32_t)(h * 2 + j);
-    float dw_acc = 0.f;
-    for (int tile = 0; tile < p.T_eff; ++tile) {
-      // masked cotangents of this warp's row for the tile
-      {
-        const int t0 = tile * kTileT + 4 * (int)lane;
-        float gv[4];
+    uint32_t acount = 0, scount = 0, icount = 0;
+    bool ok = true;
+    for (int it = blockIdx.x; it < p.n_items; it += gridDim.x, ++icount) {
+      const PairInfo pi = pair_info(p, p.n_items - 1 - it);
+      const int s = pi.s0 + j;
+      const bool row_ok = (pi.sl0 + j < p.rows) && s < p.S;
+      const int thr = j ? pi.thr1 : pi.thr0;
+      const int seg = (segs && row_ok) ? p.q_seg[(size_t)p.b * p.S + s] : 0;
+      float wc = 0.f;
+      if (row_ok) {
+        const size_t off = ((size_t)p.b * p.S + s) * kBH + h;
+        wc = (p.w_f32 ? reinterpret_cast<const float*>(p.w)[off]
+                      : __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p.w)[off])) *
+             p.scale;
+      }
+      float dw_acc = 0.f;
+      // masked cotangents of this warp's row and half for one tile (two per
+      // lane); the next tile's are loaded while the current tile is processed
+      auto load_g = [&](int tile) -> float2 {
+        const int t0 = tile * kTileT + hf * 64 + 2 * (int)lane;
+        float gv[2];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
+        for (int u = 0; u < 2; ++u) {
           const int t = t0 + u;
           bool vis = row_ok && t < thr;
           if (vis && segs) vis = p.kv_seg[(size_t)p.b * p.W + t] == seg;
           gv[u] = vis ? p.g[((size_t)p.b * p.S + s) * p.W + t] : 0.f;
         }
-        *reinterpret_cast<float4*>(gb + 4 * lane) = make_float4(gv[0], gv[1], gv[2], gv[3]);
-      }
-      __syncwarp();
-      // the staging tile of two tiles ago has been read by its TMA store
-      if (e == 0 && lane == 0) bulk_wait_group_read<1>();
-      named_bar_sync(kBEpiBar, 128);
-      uint8_t* pt = sm.ptile(tile & 1);
-      const bool computed = tile < t_hi;
-      const int a = tile & 1;
-      bool ok = true;
-      if (computed) {
-        ok = mbar_wait(sm.acc_full(a), (tile >> 1) & 1, ctl);
-        tc_fence_after();
-      }
-      float va[32], vb[32];
-      if (computed && ok) {
-        tmem_ld32_start(t_lane + (uint32_t)(a * kTileT), va);
-        tmem_wait32(va);
-      }
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {  // 32 entries per chunk
-        float(&cur)[32] = (c & 1) ? vb : va;
-        float(&nxt)[32] = (c & 1) ? va : vb;
-        if (computed && ok && c + 1 < 4) tmem_ld32_start(t_lane + (uint32_t)(a * kTileT + (c + 1) * 32), nxt);
-        uint32_t pk[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          float pr[2];
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int col = c * 32 + 2 * i + u;
-            const float x = (computed && ok) ? cur[2 * i + u] * p.scale : 0.f;
-            const float gm = gb[col];
-            dw_acc = fmaf(gm, fmaxf(x, 0.f), dw_acc);
-            pr[u] = (x > 0.f) ? gm * wc : 0.f;
-          }
-          const __nv_bfloat162 b2 = __floats2bfloat162_rn(pr[0], pr[1]);
-          pk[i] = *reinterpret_cast<const uint32_t*>(&b2);
-        }
-        // 32 entries = 64 bytes: 16-byte chunks 4*(c&1) .. 4*(c&1)+3 of half c>>1
-        uint8_t* half = pt + (c >> 1) * kBPHalf + srow * 128u;
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          const uint32_t chunk = (uint32_t)(4 * (c & 1) + q4);
-          const uint32_t pos = chunk ^ (srow & 7u);  // 128-byte swizzle
-          *reinterpret_cast<uint4*>(half + pos * 16u) =
-              make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
-        }
-        if (computed && ok && c + 1 < 4) tmem_wait32(nxt);
-      }
-      if (computed) {
-        tc_fence_before();
+        return make_float2(gv[0], gv[1]);
+      };
+      float2 g_next = (p.T_eff > 0) ? load_g(0) : make_float2(0.f, 0.f);
+      for (int tile = 0; tile < p.T_eff; ++tile, ++scount) {
+        *reinterpret_cast<float2*>(gb + 2 * lane) = g_next;
+        if (tile + 1 < p.T_eff) g_next = load_g(tile + 1);
+        // this warp's staging buffer of two stores ago has been read
+        if (lane == 0) bulk_wait_group_read<1>();
         __syncwarp();
-        if (lane == 0) mbar_arrive(sm.acc_empty(a));
+        uint8_t* stg = sm.pstage(e, (int)(scount & 1u)) + lane * 128u;
+        const bool computed = tile < pi.t_hi;
+        const int a = acount & 1;
+        if (computed && ok) {
+          ok = mbar_wait(sm.acc_full(a), (acount >> 1) & 1u, ctl);
+          tc_fence_after();
+        }
+        const bool live = computed && ok;
+        float va[32], vb[32];
+        const uint32_t col0 = (uint32_t)(a * kTileT + hf * 64);
+        if (live) {
+          tmem_ld32_start(t_lane + col0, va);
+          tmem_wait32(va);
+        }
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {  // 32 entries per chunk
+          float(&cur)[32] = (c & 1) ? vb : va;
+          float(&nxt)[32] = (c & 1) ? va : vb;
+          if (live && c == 0) tmem_ld32_start(t_lane + col0 + 32u, nxt);
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            float pr[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              const int col = c * 32 + 2 * i + u;
+              const float x = live ? cur[2 * i + u] * p.scale : 0.f;
+              const float gm = gb[col];
+              dw_acc = fmaf(gm, fmaxf(x, 0.f), dw_acc);
+              pr[u] = (x > 0.f) ? gm * wc : 0.f;
+            }
+            const __nv_bfloat162 b2 = __floats2bfloat162_rn(pr[0], pr[1]);
+            pk[i] = *reinterpret_cast<const uint32_t*>(&b2);
+          }
+          // 32 entries = 64 bytes: 16-byte chunks 4c .. 4c+3 of the row
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            const uint32_t chunk = (uint32_t)(4 * c + q4);
+            const uint32_t pos = chunk ^ (lane & 7u);  // 128-byte swizzle (row = lane)
+            *reinterpret_cast<uint4*>(stg + pos * 16u) =
+                make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
+          }
+          if (live && c == 0) tmem_wait32(nxt);
+        }
+        if (computed) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(sm.acc_empty(a));
+          ++acount;
+        }
+        fence_proxy_async_shared();
+        __syncwarp();
+        if (lane == 0 && pi.sl0 + j < p.rows) {
+          tma_store_3d(&tmap_p, sm.pstage(e, (int)(scount & 1u)), tile * kTileT + hf * 64, pi.sl0 + j, h0);
+          bulk_commit_group();
+        }
+        __syncwarp();
       }
-      fence_proxy_async_shared();
-      named_bar_sync(kBEpiBar, 128);
-      if (e == 0 && lane == 0) {
-        tma_store_3d(&tmap_p, pt, tile * kTileT, sl0, 0);
-        tma_store_3d(&tmap_p, pt + kBPHalf, tile * kTileT + 64, sl0, 0);
-        bulk_commit_group();
-      }
-      __syncwarp();
+      // dw: the second half's partial sums join the first half's (buffers
+      // alternate by pair, so one barrier per pair suffices)
+      float* dwp = sm.dwp((int)(icount & 1u));
+      if (hf == 1) dwp[m] = dw_acc;
+      named_bar_sync(kBEpiBar, 32 * kBEpiWarps);
+      if (hf == 0 && row_ok) p.dw[((size_t)p.b * p.S + s) * kBH + h] = dw_acc + dwp[m];
     }
-    if (row_ok) p.dw[((size_t)p.b * p.S + s) * kBH + h] = dw_acc;
-    if (e == 0 && lane == 0) bulk_wait_group_all();
+    if (lane == 0) bulk_wait_group_all();
   }
   __syncwarp();
   tc_fence_before();
@@ -313,7 +372,8 @@ cudaError_t launch_backward_kernel(const CUtensorMap& tq, const CUtensorMap& tk,
     configured_device = dev;
   }
   if (bp.n_items <= 0) return cudaSuccess;
-  csa_backward_kernel<<<bp.n_items, kBThreads, kBSmem, stream>>>(tq, tk, tp, bp);
+  const int grid = bp.grid < bp.n_items ? bp.grid : bp.n_items;
+  csa_backward_kernel<<<grid, kBThreads, kBSmem, stream>>>(tq, tk, tp, bp);
   return cudaGetLastError();
 }
 

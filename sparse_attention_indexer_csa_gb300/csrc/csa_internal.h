@@ -42,6 +42,7 @@ struct BwdParams {
   int s_base;   // first row of the chunk
   int rows;     // rows in the chunk
   int n_items;  // pairs of rows: (rows + 1) / 2
+  int grid;     // CTAs (persistent; at most n_items are launched)
   int T_eff;    // tiles of the chunk's GEMM range: P is written for [0, T_eff*128)
   int w_f32;
   float scale;
