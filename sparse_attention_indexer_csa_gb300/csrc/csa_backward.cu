@@ -247,7 +247,7 @@ __global__ void __launch_bounds__(kBThreads, 1)
                       : __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p.w)[off])) *
              p.scale;
       }
-      float dw_acc = 0.f;
+      float2 dw2 = make_float2(0.f, 0.f);  // dw / scale, two partial sums
       // masked cotangents of this warp's row and half for one tile (two per
       // lane); the next tile's are loaded while the current tile is processed
       auto load_g = [&](int tile) -> float2 {
@@ -288,20 +288,23 @@ __global__ void __launch_bounds__(kBThreads, 1)
           float(&cur)[32] = (c & 1) ? vb : va;
           float(&nxt)[32] = (c & 1) ? va : vb;
           if (live && c == 0) tmem_ld32_start(t_lane + col0 + 32u, nxt);
+          // scale > 0: [scale*x > 0] = [x > 0], and the scale of dw is applied once per pair
           uint32_t pk[16];
+          const float4* g4 = reinterpret_cast<const float4*>(gb + c * 32);
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            float pr[2];
+          for (int i4 = 0; i4 < 8; ++i4) {
+            const float4 gq = g4[i4];
+            const float gs[4] = {gq.x, gq.y, gq.z, gq.w};
 #pragma unroll
-            for (int u = 0; u < 2; ++u) {
-              const int col = c * 32 + 2 * i + u;
-              const float x = live ? cur[2 * i + u] * p.scale : 0.f;
-              const float gm = gb[col];
-              dw_acc = fmaf(gm, fmaxf(x, 0.f), dw_acc);
-              pr[u] = (x > 0.f) ? gm * wc : 0.f;
+            for (int i2 = 0; i2 < 2; ++i2) {
+              const int i = 2 * i4 + i2;
+              const float x0 = live ? cur[2 * i] : 0.f, x1 = live ? cur[2 * i + 1] : 0.f;
+              const float2 gm = make_float2(gs[2 * i2], gs[2 * i2 + 1]);
+              dw2 = ffma2(gm, make_float2(fmaxf(x0, 0.f), fmaxf(x1, 0.f)), dw2);
+              const float2 gw = fmul2(gm, make_float2(wc, wc));
+              const __nv_bfloat162 b2 = __floats2bfloat162_rn(x0 > 0.f ? gw.x : 0.f, x1 > 0.f ? gw.y : 0.f);
+              pk[i] = *reinterpret_cast<const uint32_t*>(&b2);
             }
-            const __nv_bfloat162 b2 = __floats2bfloat162_rn(pr[0], pr[1]);
-            pk[i] = *reinterpret_cast<const uint32_t*>(&b2);
           }
           // 32 entries = 64 bytes: 16-byte chunks 4c .. 4c+3 of the row
 #pragma unroll
@@ -329,6 +332,7 @@ __global__ void __launch_bounds__(kBThreads, 1)
       }
       // dw: the second half's partial sums join the first half's (buffers
       // alternate by pair, so one barrier per pair suffices)
+      const float dw_acc = (dw2.x + dw2.y) * p.scale;
       float* dwp = sm.dwp((int)(icount & 1u));
       if (hf == 1) dwp[m] = dw_acc;
       named_bar_sync(kBEpiBar, 32 * kBEpiWarps);

@@ -398,6 +398,17 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// Packed fp32x2 product: (a.x*b.x, a.y*b.y).
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
+  uint64_t A, B, D;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(A) : "f"(a.x), "f"(a.y));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(B) : "f"(b.x), "f"(b.y));
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(D) : "l"(A), "l"(B));
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(D));
+  return r;
+}
+
 // Packed fp32x2 FMA: (a.x*b.x + c.x, a.y*b.y + c.y).
 __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
   uint64_t A, B, C, D;
