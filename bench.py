@@ -398,6 +398,17 @@ def run_ours(args, wl, inp):
         g_bytes = gout.numel() * 2 + idx.numel() * 4 + n_sel * wl.D * 2
         line["gather"] = {"ms": g_ms, "bytes": g_bytes, "GB/s": g_bytes / (g_ms * 1e-3) / 1e9,
                           "frac_of_hbm": g_bytes / (g_ms * 1e-3) / 1e9 / float(peaks.get("hbm_gbs", 6800.0))}
+    if rank == 0 and world == 1 and not args.no_backward and wl.H == 64 and wl.D == 128 and wl.S > 2:
+        # the backward of the same scores, reported beside the forward (not in its step)
+        try:
+            b_ms, b_tf = backward_leg(wl, wk, q, k, w, q_seg, kv_seg, q_start, dev, stream, steps=20)
+            line["backward"] = {"ms_per_step": b_ms, "value": b_tf, "unit": "TFLOP/s",
+                                "frac_of_bf16_peak": b_tf / float(peaks.get("bf16_tflops",
+                                                                            FALLBACK_PEAKS["bf16_tflops"])),
+                                "steps": 20,
+                                "counts": "3 x 2*H*D per visible pair (logits recomputed, dq, dk)"}
+        except Exception as ex:  # reported, never hides the forward line
+            line["backward"] = {"error": str(ex)[:300]}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cb = oracle_sample(inp, args.cpu_seconds)
         line["cpu_baseline"] = {"value": cb["tflops"], "unit": "TFLOP/s", "cores": os.cpu_count(),
@@ -408,6 +419,41 @@ def run_ours(args, wl, inp):
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
+
+
+def backward_leg(wl, wk, q, k, w, q_seg, kv_seg, q_start, dev, stream, steps, warmup=3):
+    """Times csa_index_backward (dq, dk, dw for a fixed seeded cotangent of
+    the scores) with CUDA events on `stream`; returns (ms per step, useful
+    TFLOP/s): 3 x 2*H*D per visible pair (logits recomputed, dq, dk)."""
+    import sparse_attention_indexer_csa_gb300 as csa
+
+    gen = torch.Generator().manual_seed(wl.seed + 1000)
+    g = torch.randn(wl.B, wl.S, wl.W, generator=gen, dtype=torch.float32).to(dev)
+    p = csa.make_problem(q, k, w, wl.scale, wl.compress_rate, 1)
+    dq = torch.empty(wl.B, wl.H, wl.S, wl.D, dtype=torch.float32, device=dev)
+    dk = torch.empty(wl.B, wl.W, wl.D, dtype=torch.float32, device=dev)
+    dw = torch.empty(wl.B, wl.S, wl.H, dtype=torch.float32, device=dev)
+    ws = torch.empty(csa.workspace_size(p, 2), dtype=torch.uint8, device=dev)
+
+    def step():
+        st = csa.abi.index_backward_raw(p, q, k, w, q_seg, kv_seg, q_start, g, dq, dk, dw, ws, stream)
+        if st != csa.CSA_OK:
+            raise RuntimeError(f"csa_index_backward returned {st}")
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if csa.device_status(stream) != csa.CSA_OK:
+        raise RuntimeError("device status word reports an error after the backward")
+    ms = e0.elapsed_time(e1) / steps
+    return ms, 3.0 * wk["flops"] / (ms * 1e-3) / 1e12
 
 
 def run_backward(args, wl, inp):
@@ -427,44 +473,14 @@ def run_backward(args, wl, inp):
     q_seg = None if inp.q_seg is None else inp.q_seg.to(dev)
     kv_seg = None if inp.kv_seg is None else inp.kv_seg.to(dev)
     q_start = None if inp.q_start is None else inp.q_start.to(dev)
-    gen = torch.Generator().manual_seed(wl.seed + 1000)
-    g = torch.randn(wl.B, wl.S, wl.W, generator=gen, dtype=torch.float32).to(dev)
-    p = csa.make_problem(q, k, w, wl.scale, wl.compress_rate, 1)
-    dq = torch.empty(wl.B, wl.H, wl.S, wl.D, dtype=torch.float32, device=dev)
-    dk = torch.empty(wl.B, wl.W, wl.D, dtype=torch.float32, device=dev)
-    dw = torch.empty(wl.B, wl.S, wl.H, dtype=torch.float32, device=dev)
-    ws = torch.empty(csa.workspace_size(p, 2), dtype=torch.uint8, device=dev)
-
-    def step():
-        st = csa.abi.index_backward_raw(p, q, k, w, q_seg, kv_seg, q_start, g, dq, dk, dw, ws, stream)
-        if st != csa.CSA_OK:
-            raise RuntimeError(f"csa_index_backward returned {st}")
-
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
-    if csa.device_status(stream) != csa.CSA_OK:
-        raise RuntimeError("device status word reports an error after warm-up")
     clocks = ClockSampler(0)
     torch.cuda.synchronize()
     clocks.start()
     time.sleep(0.25)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
-        step()
-    e1.record(stream)
-    torch.cuda.synchronize()
+    ms, achieved = backward_leg(wl, wk, q, k, w, q_seg, kv_seg, q_start, dev, stream, args.steps, args.warmup)
     clk = clocks.stop()
-    ms = e0.elapsed_time(e1) / args.steps
-    if csa.device_status(stream) != csa.CSA_OK:
-        raise RuntimeError("device status word reports an error after the timed region")
-    # useful work: the logits recomputed, dq and dk, 2*H*D flops each per visible pair
-    flops = 3.0 * wk["flops"]
     peaks, peak_src = read_peaks()
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
-    achieved = flops / (ms * 1e-3) / 1e12
     line = {
         "metric": "indexer backward useful TFLOP/s (dq, dk, dw of the visible scores)", "value": achieved,
         "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
@@ -493,6 +509,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end measurement")
     ap.add_argument("--backward", action="store_true",
                     help="time the backward of the score step instead (its own JSON line)")
+    ap.add_argument("--no-backward", action="store_true",
+                    help="skip the backward measurement reported beside the forward")
     ap.add_argument("--gather", action="store_true",
                     help="also time the gather of the selected compressed rows (reported, not in the step)")
     args = ap.parse_args()

@@ -3,14 +3,16 @@ oracle's ``index_scores_vjp``.
 
 Tolerances follow from the arithmetic of the GPU path:
 * P = gm * w * scale * [x > 0] is rounded to bf16 before the dq / dk GEMMs
-  (at most 2^-9 relative per term); the GEMMs accumulate in fp32.  So
-  |dq - dq_ref| <= 2^-8 * (|P| @ |k|) per element, and likewise for dk with
-  |P|^T @ |q| summed over heads (a factor 2 above the rounding bound).
-* x = q.k comes from fp32 accumulation of bf16 products (error far below
-  1e-5 * |q|.|k|): where |scale * x| is within that margin the ReLU gate may
-  differ between fp32 and fp64, so those entries' full terms are allowed.
-* dw is accumulated in fp32 from fp32 products: 1e-5 of sum |gm| * scale *
-  |q|.|k|.
+  (8 significant bits: at most 2^-8 relative per term); the GEMMs accumulate
+  in fp32.  So |dq - dq_ref| <= 2^-7 * (|P| @ |k|) per element, and likewise
+  for dk with |P|^T @ |q| summed over heads (a factor 2 above the rounding
+  bound).
+* x = q.k comes from the tensor cores' fp32 accumulation of bf16 products
+  (error far below 1e-4 * |q|.|k|): where |x| is within that margin the ReLU
+  gate may differ between fp32 and fp64, so those entries' full terms are
+  allowed.
+* dw is accumulated in fp32 from those fp32 logits: 1e-4 of sum |gm| * scale
+  * |q|.|k| (the same envelope of the logits' error).
 Full-size problems are checked on sampled rows (dq, dw) and, for dk, by
 Euler's identity: the score is degree-1 homogeneous in q, k and w, so
 sum(q*dq), sum(k*dk) and sum(w*dw) all equal sum(g * score).
@@ -59,11 +61,11 @@ def _bounds(q, k, w, scale, r, g, q_start=None, q_seg=None, kv_seg=None, rows=No
             qb = q[b, h][rows]
             x = qb @ k[b].T
             mag = np.abs(qb) @ np.abs(k[b]).T             # |q|.|k| per pair
-            amb = np.abs(c * x) <= 1e-5 * c * mag           # ReLU gate may differ in fp32
+            amb = np.abs(x) <= 1e-4 * mag                  # ReLU gate may differ in fp32
             pabs = np.abs(gm[b]) * abs(w[b, rows, h])[:, None] * c
-            term = 2.0 ** -8 * pabs * (x > 0) + pabs * amb
+            term = 2.0 ** -7 * pabs * (x > 0) + pabs * amb
             bdq[b, h] = term @ np.abs(k[b])
-            bdw[b, :, h] = 1e-5 * (np.abs(gm[b]) * c * mag).sum(axis=1)
+            bdw[b, :, h] = 1e-4 * (np.abs(gm[b]) * c * mag).sum(axis=1)
             if bdk is not None:
                 bdk[b] += term.T @ np.abs(qb)
     floor = 1e-7
@@ -173,12 +175,13 @@ def test_backward_full_size_sampled_rows_and_euler_identity():
     sw = float((w.double() * dw.double()).sum())
     # error scale: sum |g| * sum_h |w| ReLU(scale x) = sum |P| |x|, the score
     # with |w|; bf16 rounding of P moves sum(q*dq) and sum(k*dk) by at most
-    # 2^-9 of it (bound taken with a factor 2), fp32 moves sum(w*dw) far less
+    # 2^-8 of it (bound taken with a factor 2); sum(w*dw) and sum(g*score)
+    # differ by the logits' fp32 error (two products, different orders)
     sa = csa.index_score(q, k, w.abs(), wl.scale, wl.compress_rate)
     ref = float((torch.where(vis, gd.abs(), 0.0).double() * torch.where(vis, sa, 0.0).double()).sum())
-    assert abs(sw - L) <= 1e-5 * ref
-    assert abs(sq - L) <= 2.0 ** -8 * ref
-    assert abs(sk - L) <= 2.0 ** -8 * ref
+    assert abs(sw - L) <= 1e-4 * ref
+    assert abs(sq - L) <= 2.0 ** -7 * ref
+    assert abs(sk - L) <= 2.0 ** -7 * ref
     # sampled rows of dq and dw against the oracle (the same bounds as above,
     # computed for these rows only)
     rows = np.array([0, 3, 4, 5, 777, 8191, 8192, 12345, 16383])
@@ -194,10 +197,10 @@ def test_backward_full_size_sampled_rows_and_euler_identity():
         for h in range(wl.H):
             x = Qr[b, h] @ K[b].T
             mag = np.abs(Qr[b, h]) @ np.abs(K[b]).T
-            amb = np.abs(c * x) <= 1e-5 * c * mag
+            amb = np.abs(x) <= 1e-4 * mag
             pabs = np.abs(gm[b]) * np.abs(Wt[b, rows, h])[:, None] * c
-            bq = (2.0 ** -8 * pabs * (x > 0) + pabs * amb) @ np.abs(K[b]) + 1e-7
-            bw = 1e-5 * (np.abs(gm[b]) * c * mag).sum(axis=1) + 1e-7
+            bq = (2.0 ** -7 * pabs * (x > 0) + pabs * amb) @ np.abs(K[b]) + 1e-7
+            bw = 1e-4 * (np.abs(gm[b]) * c * mag).sum(axis=1) + 1e-7
             dx = gm[b] * Wt[b, rows, h][:, None] * c * (c * x > 0)
             assert (np.abs(dq_s[b, h] - dx @ K[b]) <= bq).all(), (b, h)
             assert (np.abs(dw_s[b, :, h] - (gm[b] * np.maximum(c * x, 0)).sum(axis=1)) <= bw).all(), (b, h)
