@@ -164,7 +164,7 @@ csa_status csa_index_fused_noalloc(const csa_problem* p, const void* q, const vo
  * at masked entries are ignored); writes dq [B,H,S,D], dk [B,W,D] and
  * dw [B,S,H], all fp32, every element.  Needs `workspace`:
  * csa_index_workspace_size(p, 2) bytes (256-byte aligned), which holds P for
- * one chunk of up to 1024 query rows ([H, rows, W] bf16) and a copy of the
+ * one chunk of up to 2048 query rows ([H, rows, W] bf16) and a copy of the
  * chunk's q rows: the [B,H,S,W] tensor is never formed.  Per chunk: a
  * tensor-core kernel forms P and dw, then two library GEMMs (cuBLAS, fp32
  * accumulation) form dq and add the chunk's share of dk.  P is rounded to

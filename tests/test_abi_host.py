@@ -118,7 +118,7 @@ def _bwd(lib, p, g=FAKE, dq=FAKE, dk=FAKE, dw=FAKE, ws=FAKE, nbytes=1 << 40, q=F
 def test_backward_workspace_size():
     # P of one chunk of rows ([H, rows, W_pad] bf16) + the chunk's q rows ([H, rows, D] bf16)
     assert abi.workspace_size(_p(S=16, W=4), 2) == 64 * 16 * 128 * 2 + 64 * 16 * 128 * 2
-    assert abi.workspace_size(_p(S=16384, W=4096), 2) == 64 * 1024 * 4096 * 2 + 64 * 1024 * 128 * 2
+    assert abi.workspace_size(_p(S=16384, W=4096), 2) == 64 * 2048 * 4096 * 2 + 64 * 2048 * 128 * 2
     assert abi.workspace_size(_p(S=5, W=300), 2) == 64 * 6 * 384 * 2 + 64 * 6 * 128 * 2  # rows rounded to pairs
     assert abi.workspace_size(_p(B=0), 2) == 0
 

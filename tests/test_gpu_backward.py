@@ -142,7 +142,7 @@ def test_backward_matches_oracle(case):
 
 
 def test_backward_several_chunks():
-    # 2100 rows: chunks of 1024, 1024 and 52 rows with growing GEMM ranges
+    # 2100 rows: chunks of 2048 and 52 rows with growing GEMM ranges
     wl = WORKLOADS["prefill_4k"].with_(B=1, S=2100, W=600, seed=5, top_k=16)
     _run_and_check(make_inputs(wl), 5)
 
