@@ -189,7 +189,16 @@ __device__ void run_scheduler(const KParams& p, const Smem<C>& sm, const WaitCtl
     const int slot = it % C::SLOTS;
     mbar_wait(sm.item_empty(slot), ((it / C::SLOTS) & 1) ^ 1, ctl);
     int b, rb, c;
-    item_coords(p, item, b, rb, c);
+    if constexpr (C::FUSED) {
+      // the CTA's items alternate from both ends of its list (longest rows
+      // first, shortest last), so the cheap trivial items are interleaved
+      // with scored ones instead of leaving the tensor cores idle at the end
+      const int n_mine = (p.n_items - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
+      const int jj = (it & 1) ? (n_mine - 1 - (it >> 1)) : (it >> 1);
+      item_coords(p, (int)blockIdx.x + jj * (int)gridDim.x, b, rb, c);
+    } else {
+      item_coords(p, item, b, rb, c);
+    }
     const int s0 = rb * R;
     const long long qs0 = p.q_start ? (long long)p.q_start[b] : 0ll;
     int thr[R], seg[R], nvis[R], tfirst[R], contig[R];
