@@ -41,7 +41,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # (fused_prefill_16k_launches.md); decode_32k per step, i.e. the score launch
 # plus the selection launch, the same span the decode roofline is timed over
 # (decode_32k_launches.md).  Reset an entry to None whenever a kernel changes.
-MEASURED_TRAFFIC = {"prefill_16k": None, "decode_32k": 546.5e6}
+MEASURED_TRAFFIC = {"prefill_16k": 501.0e6, "decode_32k": 546.5e6}
 
 
 # ----------------------------------------------------------------------------- work accounting
