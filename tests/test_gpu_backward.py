@@ -132,6 +132,8 @@ def test_hand_example_exact_in_64_heads():
     dict(B=1, S=256, W=300, seed=2, w_dtype="f32"),
     dict(B=2, S=200, W=64, seed=3, docs=(2, 4)),             # packed documents: segment mask
     dict(B=2, S=40, W=700, seed=4, q_start=600),             # offset rows: every chunk spans all entries
+    dict(B=3, S=1, W=1000, seed=8, q_start=5000),            # one row per sequence (decode shape)
+    dict(B=1, S=100, W=6000, seed=9, q_start=30000),         # rows longer than 4096 entries (47 tiles)
 ])
 def test_backward_matches_oracle(case):
     case = dict(case)
