@@ -160,9 +160,9 @@ csa_status csa_index_fused_noalloc(const csa_problem* p, const void* q, const vo
  *   dw[b,s,h] = sum_t gm * ReLU(scale * x)
  *   P         = gm * w[b,s,h] * scale * [x > 0]
  *   dq[b,h,s,:] = sum_t P * k[b,t,:],   dk[b,t,:] = sum_{h,s} P * q[b,h,s,:].
- * Inputs as for csa_index_score (q head-major only); g [B,S,W] fp32 (values
- * at masked entries are ignored); writes dq [B,H,S,D], dk [B,W,D] and
- * dw [B,S,H], all fp32, every element.  Needs `workspace`:
+ * Inputs as for csa_index_score; g [B,S,W] fp32 (values at masked entries
+ * are ignored); writes dq in q's layout ([B,H,S,D] or [B,S,H,D], q_layout),
+ * dk [B,W,D] and dw [B,S,H], all fp32, every element.  Needs `workspace`:
  * csa_index_workspace_size(p, 2) bytes (256-byte aligned), which holds P for
  * one chunk of up to 2048 query rows ([H, rows, W] bf16) and a copy of the
  * chunk's q rows: the [B,H,S,W] tensor is never formed.  Per chunk: a
@@ -170,7 +170,7 @@ csa_status csa_index_fused_noalloc(const csa_problem* p, const void* q, const vo
  * accumulation) form dq and add the chunk's share of dk.  P is rounded to
  * bf16 before the GEMMs; dw is accumulated in fp32 from fp32 products.
  * Several kernels and GEMMs run on `stream` per chunk; the call returns once
- * they are enqueued.  Supported: H = 64, D = 128, CSA_Q_HEAD_MAJOR.
+ * they are enqueued.  Supported: H = 64, D = 128, either q layout.
  * Added in ABI version 102.                                              */
 csa_status csa_index_backward(const csa_problem* p, const void* q, const void* k, const void* w,
                               const int32_t* q_seg, const int32_t* kv_seg, const int64_t* q_start,

@@ -211,11 +211,11 @@ def index_fused(q, k, w, scale, compress_rate, top_k, q_seg=None, kv_seg=None, q
 
 
 def index_backward(q, k, w, scale, compress_rate, g, q_seg=None, kv_seg=None, q_start=None, workspace=None,
-                   stream=None):
-    """Gradients of sum(g * score) over the visible scores -> (dq [B,H,S,D],
-    dk [B,W,D], dw [B,S,H]), fp32, for g [B,S,W] fp32."""
-    p = make_problem(q, k, w, scale, compress_rate, 1, CSA_Q_HEAD_MAJOR)
-    dq = torch.empty(p.B, p.H, p.S, p.D, dtype=torch.float32, device=q.device)
+                   stream=None, q_layout=CSA_Q_HEAD_MAJOR):
+    """Gradients of sum(g * score) over the visible scores -> (dq in q's
+    layout, dk [B,W,D], dw [B,S,H]), fp32, for g [B,S,W] fp32."""
+    p = make_problem(q, k, w, scale, compress_rate, 1, q_layout)
+    dq = torch.empty(q.shape, dtype=torch.float32, device=q.device)
     dk = torch.empty(p.B, p.W, p.D, dtype=torch.float32, device=q.device)
     dw = torch.empty(p.B, p.S, p.H, dtype=torch.float32, device=q.device)
     if workspace is None:

@@ -335,7 +335,8 @@ csa_status csa_index_backward(const csa_problem* p, const void* q, const void* k
   if ((st = check_inputs(p, q, k, w, q_seg, kv_seg, q_start)) != CSA_OK) return st;
   if (g == nullptr || dq == nullptr || dk == nullptr || dw == nullptr) return CSA_ERR_INVALID_ARG;
   if (!aligned(g, 4) || !aligned(dq, 4) || !aligned(dk, 4) || !aligned(dw, 4)) return CSA_ERR_INVALID_ARG;
-  if (p->H != 64 || p->D != 128 || p->q_layout != CSA_Q_HEAD_MAJOR) return CSA_ERR_UNSUPPORTED;
+  if (p->H != 64 || p->D != 128) return CSA_ERR_UNSUPPORTED;
+  const bool seq_major = p->q_layout == CSA_Q_SEQ_MAJOR;
   const size_t need = backward_workspace_bytes(p);
   if (workspace == nullptr || workspace_bytes < need || !aligned(workspace, 256)) return CSA_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -354,12 +355,16 @@ csa_status csa_index_backward(const csa_problem* p, const void* q, const void* k
       // last row's), or all entries when a per-sequence offset is given (its
       // value lives on the device)
       const int w_eff = q_start ? p->W : std::min<long long>(p->W, ((long long)s0 + rows) / p->compress_rate);
-      float* dq_chunk = dq + ((size_t)b * p->H * p->S + s0) * p->D;
+      // dq in q's layout: [B,H,S,D] (rows D apart, heads S*D) or [B,S,H,D] (rows H*D, heads D)
+      float* dq_chunk = seq_major ? dq + ((size_t)b * p->S + s0) * p->H * p->D
+                                  : dq + ((size_t)b * p->H * p->S + s0) * p->D;
       float* dw_chunk = dw + ((size_t)b * p->S + s0) * p->H;
       if (w_eff == 0) {  // no visible entry in the chunk
-        if (cudaMemset2DAsync(dq_chunk, (size_t)p->S * p->D * sizeof(float), 0, (size_t)rows * p->D * sizeof(float),
-                              p->H, s) != cudaSuccess ||
-            cudaMemsetAsync(dw_chunk, 0, (size_t)rows * p->H * sizeof(float), s) != cudaSuccess)
+        const cudaError_t e1 =
+            seq_major ? cudaMemsetAsync(dq_chunk, 0, (size_t)rows * p->H * p->D * sizeof(float), s)
+                      : cudaMemset2DAsync(dq_chunk, (size_t)p->S * p->D * sizeof(float), 0,
+                                          (size_t)rows * p->D * sizeof(float), p->H, s);
+        if (e1 != cudaSuccess || cudaMemsetAsync(dw_chunk, 0, (size_t)rows * p->H * sizeof(float), s) != cudaSuccess)
           return CSA_ERR_CUDA;
         continue;
       }
@@ -389,10 +394,14 @@ csa_status csa_index_backward(const csa_problem* p, const void* q, const void* k
       bp.wait_ns = kWaitNs;
       if (launch_backward_kernel(tq, tk, tp, bp, s) != cudaSuccess) return CSA_ERR_CUDA;
       // the chunk's q rows, head by head, into one [H, rows, D] block
-      const uint8_t* qsrc = static_cast<const uint8_t*>(q) + ((size_t)b * p->H * p->S + s0) * qrow;
-      if (cudaMemcpy2DAsync(qcbuf, (size_t)rows * qrow, qsrc, (size_t)p->S * qrow, (size_t)rows * qrow, p->H,
-                            cudaMemcpyDeviceToDevice, s) != cudaSuccess)
-        return CSA_ERR_CUDA;
+      if (seq_major) {
+        if (launch_gather_q_rows(q, qcbuf, b, p->S, p->H, s0, rows, s) != cudaSuccess) return CSA_ERR_CUDA;
+      } else {
+        const uint8_t* qsrc = static_cast<const uint8_t*>(q) + ((size_t)b * p->H * p->S + s0) * qrow;
+        if (cudaMemcpy2DAsync(qcbuf, (size_t)rows * qrow, qsrc, (size_t)p->S * qrow, (size_t)rows * qrow, p->H,
+                              cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+          return CSA_ERR_CUDA;
+      }
       BwdGemms gm;
       gm.H = p->H;
       gm.D = p->D;
@@ -403,7 +412,8 @@ csa_status csa_index_backward(const csa_problem* p, const void* q, const void* k
       gm.k = static_cast<const uint8_t*>(k) + (size_t)b * p->W * qrow;
       gm.qc = qcbuf;
       gm.dq = dq_chunk;
-      gm.dq_head_stride = (long long)p->S * p->D;
+      gm.dq_head_stride = seq_major ? (long long)p->D : (long long)p->S * p->D;
+      gm.dq_row_stride = seq_major ? p->H * p->D : p->D;
       gm.dk = dk + (size_t)b * p->W * p->D;
       if (!backward_gemms(gm, s)) return CSA_ERR_CUDA;
     }

@@ -391,7 +391,7 @@ bool backward_gemms(const BwdGemms& gm, cudaStream_t stream) {
   // dq[h][rows x D] = P[h][rows x W_eff] . k[W_eff x D]   (column-major: D x rows = k^T . P^T)
   if (cublasGemmStridedBatchedEx(h, CUBLAS_OP_N, CUBLAS_OP_N, gm.D, gm.rows, gm.w_eff, &one, gm.k, CUDA_R_16BF,
                                  gm.D, 0, gm.p, CUDA_R_16BF, gm.w_pad, (long long)gm.rows * gm.w_pad, &zero, gm.dq,
-                                 CUDA_R_32F, gm.D, gm.dq_head_stride, gm.H, CUBLAS_COMPUTE_32F,
+                                 CUDA_R_32F, gm.dq_row_stride, gm.dq_head_stride, gm.H, CUBLAS_COMPUTE_32F,
                                  CUBLAS_GEMM_DEFAULT) != CUBLAS_STATUS_SUCCESS)
     return false;
   // dk[W_eff x D] += P_all^T[W_eff x (H rows)] . Q[(H rows) x D]   (column-major: D x W_eff = Q^T . P_all)
@@ -400,6 +400,28 @@ bool backward_gemms(const BwdGemms& gm, cudaStream_t stream) {
                    CUBLAS_GEMM_DEFAULT) != CUBLAS_STATUS_SUCCESS)
     return false;
   return true;
+}
+
+namespace {
+// One 256-byte row (D = 128 bf16) per 16 threads: qc[h][r] = q[b, s0+r, h].
+__global__ void csa_gather_q_rows_kernel(const uint4* __restrict__ q, uint4* __restrict__ qc, int b, int S, int H,
+                                         int s0, int rows) {
+  const long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const long long n = (long long)H * rows * 16;
+  if (gid >= n) return;
+  const int part = (int)(gid & 15), rh = (int)(gid >> 4);
+  const int h = rh / rows, r = rh % rows;
+  qc[(size_t)rh * 16 + part] = q[(((size_t)b * S + s0 + r) * H + h) * 16 + part];
+}
+}  // namespace
+
+cudaError_t launch_gather_q_rows(const void* q, void* qc, int b, int S, int H, int s0, int rows, cudaStream_t stream) {
+  const long long n = (long long)H * rows * 16;
+  if (n <= 0) return cudaSuccess;
+  const int threads = 256;
+  csa_gather_q_rows_kernel<<<(unsigned)((n + threads - 1) / threads), threads, 0, stream>>>(
+      static_cast<const uint4*>(q), static_cast<uint4*>(qc), b, S, H, s0, rows);
+  return cudaGetLastError();
 }
 
 cudaError_t take_status_backward(uint32_t* out, cudaStream_t stream) {

@@ -59,14 +59,17 @@ struct BwdGemms {
   const void* p;       // [H, rows, w_pad] bf16
   const void* k;       // [W, D] bf16 of the batch
   const void* qc;      // [H, rows, D] bf16 copy of the chunk's q rows
-  float* dq;           // dq[b, 0, s_base, 0]; heads dq_head_stride floats apart
-  long long dq_head_stride;
+  float* dq;           // dq of the chunk's first row, head 0
+  long long dq_head_stride;  // floats between heads (S*D head-major, D sequence-major)
+  int dq_row_stride;         // floats between rows (D head-major, H*D sequence-major)
   float* dk;           // dk[b] [W, D]
 };
 cudaError_t launch_backward_kernel(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tp,
                                    const BwdParams& bp, cudaStream_t stream);
 size_t backward_kernel_smem();
 bool backward_gemms(const BwdGemms& gm, cudaStream_t stream);
+// qc[h][r][:] = q[b, s0 + r, h, :] for a sequence-major q (bf16, D = 128).
+cudaError_t launch_gather_q_rows(const void* q, void* qc, int b, int S, int H, int s0, int rows, cudaStream_t stream);
 cudaError_t take_status_backward(uint32_t* out, cudaStream_t stream);
 
 // Kernel that waits on a barrier nothing completes, bounded by `ns`.

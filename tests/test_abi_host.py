@@ -132,6 +132,5 @@ def test_backward_argument_checks(lib):
     assert _bwd(lib, _p(), ws=None) == abi.CSA_ERR_INVALID_ARG
     assert _bwd(lib, _p(), nbytes=need - 1) == abi.CSA_ERR_INVALID_ARG
     assert _bwd(lib, _p(), ws=ctypes.c_void_p(0x10010)) == abi.CSA_ERR_INVALID_ARG
-    # only H=64, D=128, head-major q
+    # only H=64, D=128
     assert _bwd(lib, _p(H=4, D=32)) == abi.CSA_ERR_UNSUPPORTED
-    assert _bwd(lib, _p(q_layout=1)) == abi.CSA_ERR_UNSUPPORTED

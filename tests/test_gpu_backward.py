@@ -143,6 +143,29 @@ def test_backward_matches_oracle(case):
     _run_and_check(make_inputs(wl), seed)
 
 
+def test_backward_sequence_major_q():
+    # q [B,S,H,D]: dq comes back in the same layout and equals the head-major
+    # result within the same bounds (the oracle works on the head-major view)
+    wl = WORKLOADS["prefill_4k"].with_(B=2, S=2100, W=600, seed=10, top_k=16)
+    inp = make_inputs(wl)
+    q, k, w, qs, ks, st = _dev(inp)
+    qsm = q.transpose(1, 2).contiguous()
+    g = _cot(wl.B, wl.S, wl.W, 10)
+    dq, dk, dw = csa.index_backward(qsm, k, w, wl.scale, wl.compress_rate, g.cuda(), q_layout=csa.CSA_Q_SEQ_MAJOR)
+    torch.cuda.synchronize()
+    assert csa.device_status() == csa.CSA_OK
+    assert dq.shape == qsm.shape
+    Q, K, Wt = to_f64(inp.q), to_f64(inp.k), to_f64(inp.w)
+    G = g.double().numpy()
+    rq, rk, rw = O.index_scores_vjp(Q, K, Wt, wl.scale, wl.compress_rate, G)
+    bq, bk, bw = _bounds(Q, K, Wt, wl.scale, wl.compress_rate, G)
+    got_dq = dq.transpose(1, 2).double().cpu().numpy()
+    for name, got, ref, bd in (("dq", got_dq, rq, bq), ("dk", dk.double().cpu().numpy(), rk, bk),
+                               ("dw", dw.double().cpu().numpy(), rw, bw)):
+        bad = np.abs(got - ref) > bd
+        assert not bad.any(), f"{name}: {int(bad.sum())} elements outside bound"
+
+
 def test_backward_several_chunks():
     # 2100 rows: chunks of 2048 and 52 rows with growing GEMM ranges
     wl = WORKLOADS["prefill_4k"].with_(B=1, S=2100, W=600, seed=5, top_k=16)
