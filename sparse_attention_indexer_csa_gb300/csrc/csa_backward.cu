@@ -347,17 +347,24 @@ __global__ void __launch_bounds__(kBThreads, 1)
   if (warp == 1) tmem_dealloc(tmem_base, kBTmemCols);
 }
 
-cublasHandle_t blas_handle() {
-  static cublasHandle_t handles[64];
+// One cuBLAS handle per device, created on first use.  Setting its stream
+// and enqueueing the GEMMs happen under the device's mutex, so calls from
+// several host threads on one device do not race on the handle's stream.
+struct BlasSlot {
+  cublasHandle_t handle = nullptr;
+  std::mutex lock;
+};
+BlasSlot* blas_slot() {
+  static BlasSlot slots[64];
   static std::once_flag flags[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
   std::call_once(flags[dev], [dev] {
     cublasHandle_t h = nullptr;
     if (cublasCreate(&h) != CUBLAS_STATUS_SUCCESS) h = nullptr;
-    handles[dev] = h;
+    slots[dev].handle = h;
   });
-  return handles[dev];
+  return slots[dev].handle ? &slots[dev] : nullptr;
 }
 
 }  // namespace
@@ -385,8 +392,11 @@ cudaError_t launch_backward_kernel(const CUtensorMap& tq, const CUtensorMap& tk,
 // dk (one GEMM over all heads and rows), fp32 accumulation of bf16 operands.
 // Row-major operands are passed to the column-major library transposed.
 bool backward_gemms(const BwdGemms& gm, cudaStream_t stream) {
-  cublasHandle_t h = blas_handle();
-  if (h == nullptr || cublasSetStream(h, stream) != CUBLAS_STATUS_SUCCESS) return false;
+  BlasSlot* slot = blas_slot();
+  if (slot == nullptr) return false;
+  std::lock_guard<std::mutex> guard(slot->lock);
+  cublasHandle_t h = slot->handle;
+  if (cublasSetStream(h, stream) != CUBLAS_STATUS_SUCCESS) return false;
   const float one = 1.f, zero = 0.f;
   // dq[h][rows x D] = P[h][rows x W_eff] . k[W_eff x D]   (column-major: D x rows = k^T . P^T)
   if (cublasGemmStridedBatchedEx(h, CUBLAS_OP_N, CUBLAS_OP_N, gm.D, gm.rows, gm.w_eff, &one, gm.k, CUDA_R_16BF,
