@@ -247,7 +247,9 @@ __global__ void __launch_bounds__(kBThreads, 1)
                       : __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p.w)[off])) *
              p.scale;
       }
-      float2 dw2 = make_float2(0.f, 0.f);  // dw / scale, two partial sums
+      // dw / scale in four independent packed partial sums (eight floats)
+      float2 dwa[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+      const float2 wc2 = make_float2(wc, wc);
       // masked cotangents of this warp's row and half for one tile (two per
       // lane); the next tile's are loaded while the current tile is processed
       auto load_g = [&](int tile) -> float2 {
@@ -287,24 +289,31 @@ __global__ void __launch_bounds__(kBThreads, 1)
         for (int c = 0; c < 2; ++c) {  // 32 entries per chunk
           float(&cur)[32] = (c & 1) ? vb : va;
           float(&nxt)[32] = (c & 1) ? va : vb;
-          if (live && c == 0) tmem_ld32_start(t_lane + col0 + 32u, nxt);
-          // scale > 0: [scale*x > 0] = [x > 0], and the scale of dw is applied once per pair
           uint32_t pk[16];
-          const float4* g4 = reinterpret_cast<const float4*>(gb + c * 32);
+          if (live) {
+            if (c == 0) tmem_ld32_start(t_lane + col0 + 32u, nxt);
+            // scale > 0: [scale*x > 0] = [x > 0].  gm = g * [x > 0] gives both
+            // P = gm * w * scale and the dw term gm * x = g * ReLU(x) (the
+            // scale of dw is applied once per pair)
+            const float4* g4 = reinterpret_cast<const float4*>(gb + c * 32);
 #pragma unroll
-          for (int i4 = 0; i4 < 8; ++i4) {
-            const float4 gq = g4[i4];
-            const float gs[4] = {gq.x, gq.y, gq.z, gq.w};
+            for (int i4 = 0; i4 < 8; ++i4) {
+              const float4 gq = g4[i4];
 #pragma unroll
-            for (int i2 = 0; i2 < 2; ++i2) {
-              const int i = 2 * i4 + i2;
-              const float x0 = live ? cur[2 * i] : 0.f, x1 = live ? cur[2 * i + 1] : 0.f;
-              const float2 gm = make_float2(gs[2 * i2], gs[2 * i2 + 1]);
-              dw2 = ffma2(gm, make_float2(fmaxf(x0, 0.f), fmaxf(x1, 0.f)), dw2);
-              const float2 gw = fmul2(gm, make_float2(wc, wc));
-              const __nv_bfloat162 b2 = __floats2bfloat162_rn(x0 > 0.f ? gw.x : 0.f, x1 > 0.f ? gw.y : 0.f);
-              pk[i] = *reinterpret_cast<const uint32_t*>(&b2);
+              for (int i2 = 0; i2 < 2; ++i2) {
+                const int i = 2 * i4 + i2;
+                const float2 x = make_float2(cur[2 * i], cur[2 * i + 1]);
+                const float2 gg = i2 ? make_float2(gq.z, gq.w) : make_float2(gq.x, gq.y);
+                const float2 gm = fmul2(gg, make_float2(step_pos(x.x), step_pos(x.y)));
+                dwa[i & 3] = ffma2(gm, x, dwa[i & 3]);
+                const float2 pv = fmul2(gm, wc2);
+                const __nv_bfloat162 b2 = __floats2bfloat162_rn(pv.x, pv.y);
+                pk[i] = *reinterpret_cast<const uint32_t*>(&b2);
+              }
             }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) pk[i] = 0u;  // tile without products: P = 0
           }
           // 32 entries = 64 bytes: 16-byte chunks 4c .. 4c+3 of the row
 #pragma unroll
@@ -332,7 +341,9 @@ __global__ void __launch_bounds__(kBThreads, 1)
       }
       // dw: the second half's partial sums join the first half's (buffers
       // alternate by pair, so one barrier per pair suffices)
-      const float dw_acc = (dw2.x + dw2.y) * p.scale;
+      const float dw_acc =
+          (((dwa[0].x + dwa[0].y) + (dwa[1].x + dwa[1].y)) + ((dwa[2].x + dwa[2].y) + (dwa[3].x + dwa[3].y))) *
+          p.scale;
       float* dwp = sm.dwp((int)(icount & 1u));
       if (hf == 1) dwp[m] = dw_acc;
       named_bar_sync(kBEpiBar, 32 * kBEpiWarps);

@@ -355,6 +355,14 @@ __device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
   return r;
 }
 
+// Step function as a value: 1.0f where x > 0 (strictly; +0, -0 and NaN give
+// 0.0f), in one compare instead of a compare and a select.
+__device__ __forceinline__ float step_pos(float x) {
+  float r;
+  asm("set.gt.f32.f32 %0, %1, 0f00000000;" : "=f"(r) : "f"(x));
+  return r;
+}
+
 // Packed fp32x2 FMA: (a.x*b.x + c.x, a.y*b.y + c.y).
 __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
   uint64_t A, B, C, D;
