@@ -232,6 +232,7 @@ __global__ void __launch_bounds__(kBThreads, 1)
     const bool segs = p.q_seg != nullptr;
     const uint32_t t_lane = tmem_base + ((uint32_t)(quarter * 32) << 16);
     float* gb = sm.g(e);
+    const uint64_t p_pol = l2_policy_evict_last();
     uint32_t acount = 0, scount = 0, icount = 0;
     bool ok = true;
     for (int it = blockIdx.x; it < p.n_items; it += gridDim.x, ++icount) {
@@ -334,7 +335,10 @@ __global__ void __launch_bounds__(kBThreads, 1)
         fence_proxy_async_shared();
         __syncwarp();
         if (lane == 0 && pi.sl0 + j < p.rows) {
-          tma_store_3d(&tmap_p, sm.pstage(e, (int)(scount & 1u)), tile * kTileT + hf * 64, pi.sl0 + j, h0);
+          // evict_last: the dq and dk GEMMs that follow read P back, and the
+          // part of the chunk that stays in L2 is not read from DRAM again
+          tma_store_3d_hint(&tmap_p, sm.pstage(e, (int)(scount & 1u)), tile * kTileT + hf * 64, pi.sl0 + j, h0,
+                            p_pol);
           bulk_commit_group();
         }
         __syncwarp();

@@ -112,10 +112,11 @@ __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* m) {
 }
 
 // TMA store of a 3-D box from shared memory, tracked by the bulk async-group
-// of the issuing thread.
-__device__ __forceinline__ void tma_store_3d(const CUtensorMap* m, const void* src, int c0, int c1, int c2) {
-  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(m),
-               "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2)
+// of the issuing thread, with an L2 eviction policy for the written lines.
+__device__ __forceinline__ void tma_store_3d_hint(const CUtensorMap* m, const void* src, int c0, int c1, int c2,
+                                                  uint64_t pol) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group.L2::cache_hint [%0, {%2, %3, %4}], [%1], %5;" ::"l"(m),
+               "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2), "l"(pol)
                : "memory");
 }
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
