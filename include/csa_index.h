@@ -164,10 +164,12 @@ csa_status csa_index_fused_noalloc(const csa_problem* p, const void* q, const vo
  * are ignored); writes dq in q's layout ([B,H,S,D] or [B,S,H,D], q_layout),
  * dk [B,W,D] and dw [B,S,H], all fp32, every element.  Needs `workspace`:
  * csa_index_workspace_size(p, 2) bytes (256-byte aligned), which holds P for
- * one chunk of up to 2048 query rows ([H, rows, W] bf16) and a copy of the
- * chunk's q rows: the [B,H,S,W] tensor is never formed.  Per chunk: a
- * tensor-core kernel forms P and dw, then two library GEMMs (cuBLAS, fp32
- * accumulation) form dq and add the chunk's share of dk.  P is rounded to
+ * one chunk of up to 2048 query rows ([rows, H, W] bf16) and, for head-major
+ * q, the chunk's q rows in the same (row, head) order: the [B,H,S,W] tensor
+ * is never formed.  Per chunk: a tensor-core kernel forms P and dw, then two
+ * library GEMMs per sub-block of 512 rows (cuBLAS, fp32 accumulation) form
+ * dq and add the sub-block's share of dk; without q_start each sub-block's P
+ * and GEMMs span only the entries its last row sees.  P is rounded to
  * bf16 before the GEMMs; dw is accumulated in fp32 from fp32 products.
  * Several kernels and GEMMs run on `stream` per chunk; the call returns once
  * they are enqueued.  Supported: H = 64, D = 128, either q layout.

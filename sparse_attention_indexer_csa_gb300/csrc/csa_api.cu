@@ -131,23 +131,36 @@ bool make_k_map(CUtensorMap* m, const csa_problem* p, const void* k) {
 // Chunk buffer of the backward: P [H, rows, w_pad] bf16 as dims (w_pad, rows, H);
 // box {64, 1, 32} = 64 entries of one row for 32 heads, stored from one
 // epilogue warp's 128-byte-swizzled staging tile.
+// P of a chunk, [rows, H, w_pad] bf16: stores of 64 entries x 32 heads of one row.
 bool make_p_map(CUtensorMap* m, const void* pbuf, int rows, int w_pad, int H) {
   auto fn = encode_fn();
   if (!fn) return false;
-  cuuint64_t dims[3] = {(cuuint64_t)w_pad, (cuuint64_t)rows, (cuuint64_t)H};
-  cuuint64_t strides[2] = {(cuuint64_t)w_pad * 2, (cuuint64_t)rows * w_pad * 2};
-  cuuint32_t box[3] = {64, 1, 32};
+  cuuint64_t dims[3] = {(cuuint64_t)w_pad, (cuuint64_t)H, (cuuint64_t)rows};
+  cuuint64_t strides[2] = {(cuuint64_t)w_pad * 2, (cuuint64_t)H * w_pad * 2};
+  cuuint32_t box[3] = {64, 32, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(pbuf), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-constexpr int kBwdChunkRows = 2048;  // query rows per backward chunk (fastest of 256 .. 4096 at S = 16384, W = 4096)
+// Backward chunking.  A chunk is one launch of the P kernel; its P stays in
+// the workspace for the chunk's GEMMs.  Each GEMM sub-block of a chunk spans
+// only the entries its own last row sees, so the padding of P to a common
+// range is bounded by the sub-block, not the chunk.  At S = 16384, W = 4096
+// (timed on one GB300): sub-blocks of 2048 rows beat 256, 512, 1024 and 4096
+// (smaller ones give smaller, less efficient GEMMs; larger ones more padding),
+// and chunks of 8192 rows beat 2048 and 4096 (fewer launches, the pairs of
+// rows spread more evenly over the CTAs).
+constexpr int kBwdSubRows = 2048;
+constexpr int kBwdChunkRowsMax = 8192;
+constexpr size_t kBwdPBytesMax = (size_t)4 << 30;  // P's share of the workspace at most
 
 int bwd_chunk_rows(const csa_problem* p) {
-  const int rc = std::min(p->S, kBwdChunkRows);
-  return (rc + 1) & ~1;
+  const size_t per_row = (size_t)p->H * w_pad_of(p) * 2;  // bytes of P per query row
+  long long rc = std::min(p->S, kBwdChunkRowsMax);
+  rc = std::min<long long>(rc, std::max<long long>(2, (long long)(kBwdPBytesMax / per_row)));
+  return (int)((rc + 1) & ~1ll);
 }
 size_t round256(size_t x) { return (x + 255) & ~(size_t)255; }
 size_t bwd_p_bytes(const csa_problem* p) {
@@ -370,6 +383,8 @@ csa_status csa_index_backward(const csa_problem* p, const void* q, const void* k
       }
       CUtensorMap tp;
       if (!make_p_map(&tp, pbuf, rows, w_pad, p->H)) return CSA_ERR_CUDA;
+      // sub-blocks only where the host knows the thresholds (no per-sequence offsets)
+      const int sub = q_start ? 0 : kBwdSubRows;
       BwdParams bp;
       std::memset(&bp, 0, sizeof(bp));
       bp.B = p->B;
@@ -383,6 +398,7 @@ csa_status csa_index_backward(const csa_problem* p, const void* q, const void* k
       bp.grid = num_sms();
       if (bp.grid <= 0) return CSA_ERR_CUDA;
       bp.T_eff = (w_eff + kTileT - 1) / kTileT;
+      bp.sub_rows = sub;
       bp.w_f32 = (p->w_dtype == CSA_F32) ? 1 : 0;
       bp.scale = p->scale;
       bp.w = w;
@@ -393,29 +409,44 @@ csa_status csa_index_backward(const csa_problem* p, const void* q, const void* k
       bp.dw = dw;
       bp.wait_ns = kWaitNs;
       if (launch_backward_kernel(tq, tk, tp, bp, s) != cudaSuccess) return CSA_ERR_CUDA;
-      // the chunk's q rows, head by head, into one [H, rows, D] block
-      if (seq_major) {
+      // the chunk's q rows in P's (row, head) order: sequence-major q already
+      // is; head-major q is gathered into the workspace
+      const uint8_t* qrows = static_cast<const uint8_t*>(q) + ((size_t)b * p->S + s0) * p->H * qrow;
+      if (!seq_major) {
         if (launch_gather_q_rows(q, qcbuf, b, p->S, p->H, s0, rows, s) != cudaSuccess) return CSA_ERR_CUDA;
-      } else {
-        const uint8_t* qsrc = static_cast<const uint8_t*>(q) + ((size_t)b * p->H * p->S + s0) * qrow;
-        if (cudaMemcpy2DAsync(qcbuf, (size_t)rows * qrow, qsrc, (size_t)p->S * qrow, (size_t)rows * qrow, p->H,
-                              cudaMemcpyDeviceToDevice, s) != cudaSuccess)
-          return CSA_ERR_CUDA;
+        qrows = qcbuf;
       }
-      BwdGemms gm;
-      gm.H = p->H;
-      gm.D = p->D;
-      gm.rows = rows;
-      gm.w_eff = w_eff;
-      gm.w_pad = w_pad;
-      gm.p = pbuf;
-      gm.k = static_cast<const uint8_t*>(k) + (size_t)b * p->W * qrow;
-      gm.qc = qcbuf;
-      gm.dq = dq_chunk;
-      gm.dq_head_stride = seq_major ? (long long)p->D : (long long)p->S * p->D;
-      gm.dq_row_stride = seq_major ? p->H * p->D : p->D;
-      gm.dk = dk + (size_t)b * p->W * p->D;
-      if (!backward_gemms(gm, s)) return CSA_ERR_CUDA;
+      const int dq_row_stride = seq_major ? p->H * p->D : p->D;
+      const int step = sub > 0 ? sub : rows;
+      for (int r0 = 0; r0 < rows; r0 += step) {
+        const int rows_i = std::min(step, rows - r0);
+        // the same range as pair_tiles() gives the sub-block's pairs
+        const int w_i = sub > 0 ? (int)std::min<long long>(p->W, ((long long)s0 + r0 + rows_i) / p->compress_rate)
+                                : w_eff;
+        float* dq_i = dq_chunk + (size_t)r0 * dq_row_stride;
+        if (w_i == 0) {  // no visible entry in the sub-block: P was not written, dq is zero
+          const cudaError_t e1 =
+              seq_major ? cudaMemsetAsync(dq_i, 0, (size_t)rows_i * p->H * p->D * sizeof(float), s)
+                        : cudaMemset2DAsync(dq_i, (size_t)p->S * p->D * sizeof(float), 0,
+                                            (size_t)rows_i * p->D * sizeof(float), p->H, s);
+          if (e1 != cudaSuccess) return CSA_ERR_CUDA;
+          continue;
+        }
+        BwdGemms gm;
+        gm.H = p->H;
+        gm.D = p->D;
+        gm.rows = rows_i;
+        gm.w_eff = w_i;
+        gm.w_pad = w_pad;
+        gm.p = pbuf + (size_t)r0 * p->H * w_pad * 2;
+        gm.k = static_cast<const uint8_t*>(k) + (size_t)b * p->W * qrow;
+        gm.qc = qrows + (size_t)r0 * p->H * qrow;
+        gm.dq = dq_i;
+        gm.dq_head_stride = seq_major ? (long long)p->D : (long long)p->S * p->D;
+        gm.dq_row_stride = dq_row_stride;
+        gm.dk = dk + (size_t)b * p->W * p->D;
+        if (!backward_gemms(gm, s)) return CSA_ERR_CUDA;
+      }
     }
   }
   return CSA_OK;

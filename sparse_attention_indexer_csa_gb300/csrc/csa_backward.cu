@@ -95,10 +95,22 @@ __device__ __forceinline__ int row_threshold(const BwdParams& p, int s) {
   return (int)tv;
 }
 
+// Tiles of P written for the pair whose first row is sl0 (relative): the GEMM
+// range of its sub-block of rows, the same expression the host uses for that
+// sub-block's GEMMs; the chunk's range without sub-blocks.
+__device__ __forceinline__ int pair_tiles(const BwdParams& p, int sl0) {
+  if (p.sub_rows <= 0) return p.T_eff;
+  const int end = min(p.rows, (sl0 / p.sub_rows + 1) * p.sub_rows);
+  long long tv = ((long long)p.s_base + end) / p.r;
+  tv = tv > p.W ? p.W : tv;
+  return (int)((tv + kTileT - 1) / kTileT);
+}
+
 // Pair number `pair` of the chunk: its first row (relative and absolute), the
-// visible thresholds of its two rows and the tiles that need products.
+// visible thresholds of its two rows, the tiles of P it writes and the tiles
+// that need products.
 struct PairInfo {
-  int sl0, s0, thr0, thr1, t_hi;
+  int sl0, s0, thr0, thr1, T, t_hi;
 };
 __device__ __forceinline__ PairInfo pair_info(const BwdParams& p, int pair) {
   PairInfo pi;
@@ -106,7 +118,8 @@ __device__ __forceinline__ PairInfo pair_info(const BwdParams& p, int pair) {
   pi.s0 = p.s_base + pi.sl0;
   pi.thr0 = row_threshold(p, pi.s0);
   pi.thr1 = (pi.sl0 + 1 < p.rows) ? row_threshold(p, pi.s0 + 1) : 0;
-  pi.t_hi = min(p.T_eff, (max(pi.thr0, pi.thr1) + kTileT - 1) / kTileT);
+  pi.T = pair_tiles(p, pi.sl0);
+  pi.t_hi = min(pi.T, (max(pi.thr0, pi.thr1) + kTileT - 1) / kTileT);
   return pi;
 }
 
@@ -265,10 +278,10 @@ __global__ void __launch_bounds__(kBThreads, 1)
         }
         return make_float2(gv[0], gv[1]);
       };
-      float2 g_next = (p.T_eff > 0) ? load_g(0) : make_float2(0.f, 0.f);
-      for (int tile = 0; tile < p.T_eff; ++tile, ++scount) {
+      float2 g_next = (pi.T > 0) ? load_g(0) : make_float2(0.f, 0.f);
+      for (int tile = 0; tile < pi.T; ++tile, ++scount) {
         *reinterpret_cast<float2*>(gb + 2 * lane) = g_next;
-        if (tile + 1 < p.T_eff) g_next = load_g(tile + 1);
+        if (tile + 1 < pi.T) g_next = load_g(tile + 1);
         // this warp's staging buffer of two stores ago has been read
         if (lane == 0) bulk_wait_group_read<1>();
         __syncwarp();
@@ -337,7 +350,7 @@ __global__ void __launch_bounds__(kBThreads, 1)
         if (lane == 0 && pi.sl0 + j < p.rows) {
           // evict_last: the dq and dk GEMMs that follow read P back, and the
           // part of the chunk that stays in L2 is not read from DRAM again
-          tma_store_3d_hint(&tmap_p, sm.pstage(e, (int)(scount & 1u)), tile * kTileT + hf * 64, pi.sl0 + j, h0,
+          tma_store_3d_hint(&tmap_p, sm.pstage(e, (int)(scount & 1u)), tile * kTileT + hf * 64, h0, pi.sl0 + j,
                             p_pol);
           bulk_commit_group();
         }
@@ -413,13 +426,15 @@ bool backward_gemms(const BwdGemms& gm, cudaStream_t stream) {
   cublasHandle_t h = slot->handle;
   if (cublasSetStream(h, stream) != CUBLAS_STATUS_SUCCESS) return false;
   const float one = 1.f, zero = 0.f;
-  // dq[h][rows x D] = P[h][rows x W_eff] . k[W_eff x D]   (column-major: D x rows = k^T . P^T)
+  // dq[h][rows x D] = P[:, h][rows x W_eff] . k[W_eff x D]   (column-major: D x rows = k^T . P^T);
+  // the rows of head h are H * w_pad apart in P, the heads w_pad apart
   if (cublasGemmStridedBatchedEx(h, CUBLAS_OP_N, CUBLAS_OP_N, gm.D, gm.rows, gm.w_eff, &one, gm.k, CUDA_R_16BF,
-                                 gm.D, 0, gm.p, CUDA_R_16BF, gm.w_pad, (long long)gm.rows * gm.w_pad, &zero, gm.dq,
+                                 gm.D, 0, gm.p, CUDA_R_16BF, gm.H * gm.w_pad, (long long)gm.w_pad, &zero, gm.dq,
                                  CUDA_R_32F, gm.dq_row_stride, gm.dq_head_stride, gm.H, CUBLAS_COMPUTE_32F,
                                  CUBLAS_GEMM_DEFAULT) != CUBLAS_STATUS_SUCCESS)
     return false;
-  // dk[W_eff x D] += P_all^T[W_eff x (H rows)] . Q[(H rows) x D]   (column-major: D x W_eff = Q^T . P_all)
+  // dk[W_eff x D] += P_all^T[W_eff x (rows H)] . Q[(rows H) x D]   (column-major: D x W_eff = Q^T . P_all),
+  // P_all and Q with their rows in the same (row, head) order
   if (cublasGemmEx(h, CUBLAS_OP_N, CUBLAS_OP_T, gm.D, gm.w_eff, gm.H * gm.rows, &one, gm.qc, CUDA_R_16BF, gm.D,
                    gm.p, CUDA_R_16BF, gm.w_pad, &one, gm.dk, CUDA_R_32F, gm.D, CUBLAS_COMPUTE_32F,
                    CUBLAS_GEMM_DEFAULT) != CUBLAS_STATUS_SUCCESS)
@@ -428,15 +443,16 @@ bool backward_gemms(const BwdGemms& gm, cudaStream_t stream) {
 }
 
 namespace {
-// One 256-byte row (D = 128 bf16) per 16 threads: qc[h][r] = q[b, s0+r, h].
+// One 256-byte row (D = 128 bf16) per 16 threads: qc[r][h] = q[b, h, s0+r]
+// (head-major q rows in the (row, head) order of P's rows).
 __global__ void csa_gather_q_rows_kernel(const uint4* __restrict__ q, uint4* __restrict__ qc, int b, int S, int H,
                                          int s0, int rows) {
   const long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   const long long n = (long long)H * rows * 16;
   if (gid >= n) return;
   const int part = (int)(gid & 15), rh = (int)(gid >> 4);
-  const int h = rh / rows, r = rh % rows;
-  qc[(size_t)rh * 16 + part] = q[(((size_t)b * S + s0 + r) * H + h) * 16 + part];
+  const int r = rh / H, h = rh % H;
+  qc[(size_t)rh * 16 + part] = q[(((size_t)b * H + h) * S + s0 + r) * 16 + part];
 }
 }  // namespace
 

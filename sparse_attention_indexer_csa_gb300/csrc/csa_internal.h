@@ -44,6 +44,8 @@ struct BwdParams {
   int n_items;  // pairs of rows: (rows + 1) / 2
   int grid;     // CTAs (persistent; at most n_items are launched)
   int T_eff;    // tiles of the chunk's GEMM range: P is written for [0, T_eff*128)
+  int sub_rows; // > 0: rows of a GEMM sub-block (even); a pair's P spans its sub-block's
+                // range, ceil(min(W, (s_base + end of sub-block) / r) / 128) tiles
   int w_f32;
   float scale;
   const void* w;
@@ -55,11 +57,11 @@ struct BwdParams {
   unsigned long long wait_ns;
 };
 struct BwdGemms {
-  int H, D, rows, w_eff, w_pad;
-  const void* p;       // [H, rows, w_pad] bf16
+  int H, D, rows, w_eff, w_pad;  // rows and GEMM range of one sub-block of a chunk
+  const void* p;       // P rows of the sub-block: [rows, H, w_pad] bf16
   const void* k;       // [W, D] bf16 of the batch
-  const void* qc;      // [H, rows, D] bf16 copy of the chunk's q rows
-  float* dq;           // dq of the chunk's first row, head 0
+  const void* qc;      // the sub-block's q rows in the same (row, head) order: [rows, H, D] bf16
+  float* dq;           // dq of the sub-block's first row, head 0
   long long dq_head_stride;  // floats between heads (S*D head-major, D sequence-major)
   int dq_row_stride;         // floats between rows (D head-major, H*D sequence-major)
   float* dk;           // dk[b] [W, D]

@@ -116,10 +116,13 @@ def _bwd(lib, p, g=FAKE, dq=FAKE, dk=FAKE, dw=FAKE, ws=FAKE, nbytes=1 << 40, q=F
 
 
 def test_backward_workspace_size():
-    # P of one chunk of rows ([H, rows, W_pad] bf16) + the chunk's q rows ([H, rows, D] bf16)
+    # P of one chunk of rows ([rows, H, W_pad] bf16) + the chunk's q rows ([rows, H, D] bf16); a chunk
+    # is at most 8192 rows and its P at most 4 GiB
     assert abi.workspace_size(_p(S=16, W=4), 2) == 64 * 16 * 128 * 2 + 64 * 16 * 128 * 2
-    assert abi.workspace_size(_p(S=16384, W=4096), 2) == 64 * 2048 * 4096 * 2 + 64 * 2048 * 128 * 2
+    assert abi.workspace_size(_p(S=16384, W=4096), 2) == 64 * 8192 * 4096 * 2 + 64 * 8192 * 128 * 2
     assert abi.workspace_size(_p(S=5, W=300), 2) == 64 * 6 * 384 * 2 + 64 * 6 * 128 * 2  # rows rounded to pairs
+    # wide rows: 4 GiB / (64 heads x 32768 entries x 2 bytes) = 1024 rows per chunk
+    assert abi.workspace_size(_p(S=16384, W=32768), 2) == 64 * 1024 * 32768 * 2 + 64 * 1024 * 128 * 2
     assert abi.workspace_size(_p(B=0), 2) == 0
 
 

@@ -166,9 +166,11 @@ def test_backward_sequence_major_q():
         assert not bad.any(), f"{name}: {int(bad.sum())} elements outside bound"
 
 
-def test_backward_several_chunks():
-    # 2100 rows: chunks of 2048 and 52 rows with growing GEMM ranges
-    wl = WORKLOADS["prefill_4k"].with_(B=1, S=2100, W=600, seed=5, top_k=16)
+@pytest.mark.parametrize("S", [2100, 8300])
+def test_backward_several_chunks(S):
+    # 2100 rows: one chunk, GEMM sub-blocks of 2048 and 52 rows with growing
+    # ranges; 8300 rows: a chunk of 8192 rows (four sub-blocks) and one of 108
+    wl = WORKLOADS["prefill_4k"].with_(B=1, S=S, W=600, seed=5, top_k=16)
     _run_and_check(make_inputs(wl), 5)
 
 
