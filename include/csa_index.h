@@ -164,7 +164,8 @@ csa_status csa_index_fused_noalloc(const csa_problem* p, const void* q, const vo
  * are ignored); writes dq in q's layout ([B,H,S,D] or [B,S,H,D], q_layout),
  * dk [B,W,D] and dw [B,S,H], all fp32, every element.  Needs `workspace`:
  * csa_index_workspace_size(p, 2) bytes (256-byte aligned), which holds P for
- * one chunk of up to 2048 query rows ([rows, H, W] bf16) and, for head-major
+ * one chunk of up to 8192 query rows ([rows, H, W] bf16, at most 4 GiB;
+ * fewer rows when W is large) and, for head-major
  * q, the chunk's q rows in the same (row, head) order: the [B,H,S,W] tensor
  * is never formed.  Per chunk: a tensor-core kernel forms P and dw, then two
  * library GEMMs per sub-block of 512 rows (cuBLAS, fp32 accumulation) form

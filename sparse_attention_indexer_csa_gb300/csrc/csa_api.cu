@@ -128,10 +128,9 @@ bool make_k_map(CUtensorMap* m, const csa_problem* p, const void* k) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Chunk buffer of the backward: P [H, rows, w_pad] bf16 as dims (w_pad, rows, H);
-// box {64, 1, 32} = 64 entries of one row for 32 heads, stored from one
+// Chunk buffer of the backward: P [rows, H, w_pad] bf16 as dims (w_pad, H, rows);
+// box {64, 32, 1} = 64 entries of one row for 32 heads, stored from one
 // epilogue warp's 128-byte-swizzled staging tile.
-// P of a chunk, [rows, H, w_pad] bf16: stores of 64 entries x 32 heads of one row.
 bool make_p_map(CUtensorMap* m, const void* pbuf, int rows, int w_pad, int H) {
   auto fn = encode_fn();
   if (!fn) return false;

@@ -9,9 +9,11 @@
 //   dq[b,h,s,:] = sum_t P * k[b,t,:]         dk[b,t,:] = sum_{h,s} P * q[b,h,s,:]
 // with gm = g on visible entries and 0 on masked ones (masked scores are
 // constants).  For a chunk of rows this kernel recomputes x on the tensor
-// cores, forms P in bf16 for the chunk only ([H, rows, W_pad] in the caller's
+// cores, forms P in bf16 for the chunk only ([rows, H, W_pad] in the caller's
 // workspace -- never the whole [B,H,S,W]) and dw in registers; dq and dk are
-// then two plain GEMMs over that chunk (cuBLAS).
+// then two plain GEMMs per sub-block of the chunk's rows (cuBLAS), each over
+// the entries the sub-block's last row sees -- the range of P a pair of rows
+// writes here.
 //
 // Kernel layout (persistent: each CTA takes pairs of query rows in turn, 320
 // threads):
@@ -26,11 +28,11 @@
 //           64 entries per tile: dw in a register (the halves added once per
 //           pair), P converted to bf16 into the warp's own 128-byte-swizzled
 //           staging tile (32 heads x 64 entries), which lane 0 writes out
-//           with a 3-D TMA store (box {64 entries, 1 row, 32 heads}); each
+//           with a 3-D TMA store (box {64 entries, 32 heads, 1 row}); each
 //           warp double-buffers its staging, so the warps never wait for
 //           one another inside a tile.
-// Tiles past the pair's visible range but inside the chunk's GEMM range are
-// written as zeros without any product.
+// Tiles past the pair's visible range but inside its sub-block's GEMM range
+// are written as zeros without any product.
 #include <cublas_v2.h>
 #include <cuda_bf16.h>
 
