@@ -406,15 +406,14 @@ csa_status csa_index_backward(const csa_problem* p, const void* q, const void* k
       bp.q_start = q_start;
       bp.g = g;
       bp.dw = dw;
+      // the chunk's q rows in P's (row, head) order: sequence-major q already
+      // is; for head-major q the kernel copies them into the workspace
+      bp.q_gather = seq_major ? nullptr : q;
+      bp.qc = seq_major ? nullptr : qcbuf;
       bp.wait_ns = kWaitNs;
       if (launch_backward_kernel(tq, tk, tp, bp, s) != cudaSuccess) return CSA_ERR_CUDA;
-      // the chunk's q rows in P's (row, head) order: sequence-major q already
-      // is; head-major q is gathered into the workspace
-      const uint8_t* qrows = static_cast<const uint8_t*>(q) + ((size_t)b * p->S + s0) * p->H * qrow;
-      if (!seq_major) {
-        if (launch_gather_q_rows(q, qcbuf, b, p->S, p->H, s0, rows, s) != cudaSuccess) return CSA_ERR_CUDA;
-        qrows = qcbuf;
-      }
+      const uint8_t* qrows = seq_major ? static_cast<const uint8_t*>(q) + ((size_t)b * p->S + s0) * p->H * qrow
+                                       : static_cast<const uint8_t*>(qcbuf);
       const int dq_row_stride = seq_major ? p->H * p->D : p->D;
       const int step = sub > 0 ? sub : rows;
       for (int r0 = 0; r0 < rows; r0 += step) {

@@ -15,7 +15,7 @@
 // the entries the sub-block's last row sees -- the range of P a pair of rows
 // writes here.
 //
-// Kernel layout (persistent: each CTA takes pairs of query rows in turn, 320
+// Kernel layout (persistent: each CTA takes pairs of query rows in turn, 352
 // threads):
 //   warp 0  TMA: per pair the q block (2 rows x 64 heads x 128, as the UMMA A
 //           operand: M = 128 rows (row j, head h) -> 64 j + h), then its k
@@ -31,6 +31,8 @@
 //           with a 3-D TMA store (box {64 entries, 32 heads, 1 row}); each
 //           warp double-buffers its staging, so the warps never wait for
 //           one another inside a tile.
+//   warp 10  for head-major q, copies the chunk's q rows into P's (row, head)
+//           order (the dk GEMMs' operand) while the other warps form P.
 // Tiles past the pair's visible range but inside its sub-block's GEMM range
 // are written as zeros without any product.
 #include <cublas_v2.h>
@@ -55,7 +57,8 @@ constexpr int kBStages = 3;
 constexpr uint32_t kBPWarp = 32 * 128;              // 4 KB: one warp's 32 heads x 64 entries of bf16
 constexpr uint32_t kBIdesc = idesc_bf16_f32(kBM, kTileT);
 constexpr int kBEpiWarps = 8;
-constexpr int kBThreads = 64 + 32 * kBEpiWarps;
+constexpr int kBGatherWarp = 2 + kBEpiWarps;       // copies the chunk's head-major q rows
+constexpr int kBThreads = 64 + 32 * kBEpiWarps + 32;
 constexpr uint32_t kBTmemCols = 256;                // two 128-column accumulators
 constexpr uint32_t kBEpiBar = 2;                    // named barrier of the epilogue warps
 
@@ -235,7 +238,7 @@ __global__ void __launch_bounds__(kBThreads, 1)
         if (!ok) break;
       }
     }
-  } else {
+  } else if (warp < kBGatherWarp) {
     // epilogue: thread = TMEM lane m = 32*quarter + lane = (row j, head h);
     // warp half hf takes entries hf*64 .. hf*64+63 of every tile
     const int e = warp - 2;
@@ -369,6 +372,32 @@ __global__ void __launch_bounds__(kBThreads, 1)
       if (hf == 0 && row_ok) p.dw[((size_t)p.b * p.S + s) * kBH + h] = dw_acc + dwp[m];
     }
     if (lane == 0) bulk_wait_group_all();
+  } else if (p.qc != nullptr) {
+    // head-major q: the chunk's q rows in P's (row, head) order for the dk
+    // GEMMs, as plain 16-byte copies spread over the CTAs while the other
+    // warps form P (eight loads in flight per lane)
+    const uint4* src = static_cast<const uint4*>(p.q_gather);
+    uint4* dst = static_cast<uint4*>(p.qc);
+    const long long n = (long long)p.rows * kBH * 16;  // 16 x 16 bytes per row of 128 bf16
+    const long long stride = (long long)gridDim.x * 32;
+    constexpr int U = 8;
+    for (long long i0 = (long long)blockIdx.x * 32 + lane; i0 < n; i0 += stride * U) {
+      uint4 v[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const long long i = i0 + u * stride;
+        if (i < n) {
+          const long long rh = i >> 4;
+          const int r = (int)(rh / kBH), hh = (int)(rh % kBH);
+          v[u] = src[(((size_t)p.b * kBH + hh) * p.S + p.s_base + r) * 16 + (i & 15)];
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const long long i = i0 + u * stride;
+        if (i < n) dst[i] = v[u];
+      }
+    }
   }
   __syncwarp();
   tc_fence_before();
@@ -442,29 +471,6 @@ bool backward_gemms(const BwdGemms& gm, cudaStream_t stream) {
                    CUBLAS_GEMM_DEFAULT) != CUBLAS_STATUS_SUCCESS)
     return false;
   return true;
-}
-
-namespace {
-// One 256-byte row (D = 128 bf16) per 16 threads: qc[r][h] = q[b, h, s0+r]
-// (head-major q rows in the (row, head) order of P's rows).
-__global__ void csa_gather_q_rows_kernel(const uint4* __restrict__ q, uint4* __restrict__ qc, int b, int S, int H,
-                                         int s0, int rows) {
-  const long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  const long long n = (long long)H * rows * 16;
-  if (gid >= n) return;
-  const int part = (int)(gid & 15), rh = (int)(gid >> 4);
-  const int r = rh / H, h = rh % H;
-  qc[(size_t)rh * 16 + part] = q[(((size_t)b * H + h) * S + s0 + r) * 16 + part];
-}
-}  // namespace
-
-cudaError_t launch_gather_q_rows(const void* q, void* qc, int b, int S, int H, int s0, int rows, cudaStream_t stream) {
-  const long long n = (long long)H * rows * 16;
-  if (n <= 0) return cudaSuccess;
-  const int threads = 256;
-  csa_gather_q_rows_kernel<<<(unsigned)((n + threads - 1) / threads), threads, 0, stream>>>(
-      static_cast<const uint4*>(q), static_cast<uint4*>(qc), b, S, H, s0, rows);
-  return cudaGetLastError();
 }
 
 cudaError_t take_status_backward(uint32_t* out, cudaStream_t stream) {

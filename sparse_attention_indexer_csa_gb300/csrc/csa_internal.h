@@ -54,6 +54,8 @@ struct BwdParams {
   const int64_t* q_start;
   const float* g;
   float* dw;
+  const void* q_gather;  // head-major q [B,H,S,D] to copy into qc, or null
+  void* qc;              // the chunk's q rows in (row, head) order [rows, H, D], or null
   unsigned long long wait_ns;
 };
 struct BwdGemms {
@@ -71,7 +73,6 @@ cudaError_t launch_backward_kernel(const CUtensorMap& tq, const CUtensorMap& tk,
 size_t backward_kernel_smem();
 bool backward_gemms(const BwdGemms& gm, cudaStream_t stream);
 // qc[h][r][:] = q[b, s0 + r, h, :] for a sequence-major q (bf16, D = 128).
-cudaError_t launch_gather_q_rows(const void* q, void* qc, int b, int S, int H, int s0, int rows, cudaStream_t stream);
 cudaError_t take_status_backward(uint32_t* out, cudaStream_t stream);
 
 // Kernel that waits on a barrier nothing completes, bounded by `ns`.
