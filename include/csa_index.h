@@ -165,15 +165,17 @@ csa_status csa_index_fused_noalloc(const csa_problem* p, const void* q, const vo
  * dk [B,W,D] and dw [B,S,H], all fp32, every element.  Needs `workspace`:
  * csa_index_workspace_size(p, 2) bytes (256-byte aligned), which holds P for
  * one chunk of up to 8192 query rows ([rows, H, W] bf16, at most 4 GiB;
- * fewer rows when W is large) and, for head-major
- * q, the chunk's q rows in the same (row, head) order: the [B,H,S,W] tensor
- * is never formed.  Per chunk: a tensor-core kernel forms P and dw, then two
- * library GEMMs per sub-block of 512 rows (cuBLAS, fp32 accumulation) form
- * dq and add the sub-block's share of dk; without q_start each sub-block's P
- * and GEMMs span only the entries its last row sees.  P is rounded to
+ * fewer rows when W is large) and, for head-major q, the chunk's q rows in
+ * the same (row, head) order: the [B,H,S,W] tensor is never formed.  Per
+ * chunk: a tensor-core kernel forms P and dw, then two library GEMMs per
+ * sub-block of 2048 rows (cuBLAS, fp32 accumulation) form dq and add the
+ * sub-block's share of dk; without q_start each sub-block's P and GEMMs span
+ * only the entries its last row sees.  P is rounded to
  * bf16 before the GEMMs; dw is accumulated in fp32 from fp32 products.
  * Several kernels and GEMMs run on `stream` per chunk; the call returns once
- * they are enqueued.  Supported: H = 64, D = 128, either q layout.
+ * they are enqueued.  The first call on a device creates the library's
+ * cuBLAS handle for that device (cuBLAS allocates its own workspace then);
+ * later calls allocate nothing.  Supported: H = 64, D = 128, either q layout.
  * Added in ABI version 102.                                              */
 csa_status csa_index_backward(const csa_problem* p, const void* q, const void* k, const void* w,
                               const int32_t* q_seg, const int32_t* kv_seg, const int64_t* q_start,
