@@ -17,8 +17,11 @@ the slowest rank's time.  ``--impl reference`` times the CPU oracle instead.
 from __future__ import annotations
 
 import argparse
+import glob
+import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -36,13 +39,40 @@ from csa_inputs import WORKLOADS, Inputs, make_inputs  # noqa: E402
 
 METRIC = "indexer useful TFLOP/s and query rows/s at S=16K; % of bf16 tensor peak"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-# DRAM bytes (read + write) per timed unit, from the ncu launch lists
-# summarised in profiles/: prefill_16k per launch of the fused kernel
-# (fused_prefill_16k_launches.md); decode_32k per step, i.e. the score launch
-# plus the selection launch, the same span the decode roofline is timed over
-# (decode_32k_launches.md).  Reset an entry to None whenever a kernel changes.
-MEASURED_TRAFFIC = {"prefill_16k": 501.0e6, "decode_32k": 546.5e6}
+# DRAM bytes (read + write) per timed unit come from the ncu launch lists
+# summarised in profiles/: each summary carries a line
+#     bench-traffic: <workload> <bytes> sources=<hash>
+# (prefill_16k: per launch of the fused kernel; decode_32k: per step, the
+# score launch plus the selection launch, the span its roofline is timed
+# over).  <hash> is forward_sources_hash() of the build that was profiled; a
+# figure whose hash differs from the current sources is stale and reported
+# as null.
+FORWARD_SOURCES = ("csa_ptx.cuh", "csa_select.cuh", "csa_score_kernel.cuh", "csa_prefill.cu", "csa_topk.cu",
+                   "csa_api.cu", "csa_internal.h")
 
+
+def forward_sources_hash() -> str:
+    """Hash of the sources of the forward kernels and their launch code."""
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "sparse_attention_indexer_csa_gb300", "csrc")
+    for name in FORWARD_SOURCES:
+        h.update(name.encode())
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:12]
+
+
+def measured_traffic(workload: str):
+    """DRAM bytes per timed unit of `workload` from profiles/, or None."""
+    pat = re.compile(r"^bench-traffic:\s+(\S+)\s+([0-9.eE+]+)\s+sources=(\w+)")
+    cur = forward_sources_hash()
+    for path in sorted(glob.glob(os.path.join(ROOT, "profiles", "*.md"))):
+        with open(path) as f:
+            for line in f:
+                m = pat.match(line.strip())
+                if m and m.group(1) == workload and m.group(3) == cur:
+                    return float(m.group(2))
+    return None
 
 # ----------------------------------------------------------------------------- work accounting
 def visible_counts(inp: Inputs) -> np.ndarray:
@@ -384,11 +414,10 @@ def run_ours(args, wl, inp):
     achieved = wk["flops_nontrivial"] / (avg_launch_ms * 1e-3) / 1e12
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     bound, unit = "tensor", "TFLOP/s"
-    traffic = MEASURED_TRAFFIC.get(wl.name) if args.batch is None else None
+    traffic = measured_traffic(wl.name) if args.batch is None else None
     if wl.name.startswith("decode"):
         # k streaming bound: algorithmic bytes = k + q + w + scores write/read + idx
-        bytes_alg = (wl.B * wl.W * wl.D * 2 + wl.B * wl.H * wl.S * wl.D * 2 + wl.B * wl.S * wl.H * 2
-                     + 2 * wl.B * wl.S * wl.W * 4 + wl.B * wl.S * wl.top_k * 4)
+        bytes_alg = decode_bytes(wl)
         achieved = bytes_alg / (avg_launch_ms * 1e-3) / 1e9
         peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
         bound, unit = "hbm", "GB/s"
@@ -443,6 +472,15 @@ def run_ours(args, wl, inp):
                                 "counts": "3 x 2*H*D per visible pair (logits recomputed, dq, dk)"}
         except Exception as ex:  # reported, never hides the forward line
             line["backward"] = {"error": str(ex)[:300]}
+    if rank == 0 and world == 1 and not args.no_side and args.batch is None and wl.name == "prefill_16k":
+        # the other two targets, each timed on its own beside the headline
+        # workload: decode (HBM-bound) and packed documents at a seed whose
+        # rows include some above top_k (seed 0 has none)
+        for key, side in (("decode", WORKLOADS["decode_32k"]), ("packed", WORKLOADS["packed_8k"].with_(seed=1))):
+            try:
+                line[key] = side_leg(side, dev, stream)
+            except Exception as ex:  # reported, never hides the headline line
+                line[key] = {"error": str(ex)[:300]}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cb = oracle_sample(inp, args.cpu_seconds)
         line["cpu_baseline"] = {"value": cb["tflops"], "unit": "TFLOP/s", "cores": os.cpu_count(),
@@ -453,6 +491,73 @@ def run_ours(args, wl, inp):
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
+
+
+def side_leg(wl, dev, stream, steps=50, warmup=5):
+    """Times csa_index_fused on another workload with CUDA events on `stream`
+    (inputs resident; each is larger than L2, so no flush is needed) and
+    returns its figures for a sub-object of the bench line."""
+    import sparse_attention_indexer_csa_gb300 as csa
+
+    inp = make_inputs(wl)
+    wk = work(inp)
+    g = lambda t: None if t is None else t.to(dev)  # noqa: E731
+    q, k, w, qs, ks, st = g(inp.q), g(inp.k), g(inp.w), g(inp.q_seg), g(inp.kv_seg), g(inp.q_start)
+    p = csa.make_problem(q, k, w, wl.scale, wl.compress_rate, wl.top_k)
+    idx = torch.empty(wl.B, wl.S, wl.top_k, dtype=torch.int32, device=dev)
+    nb = csa.workspace_size(p, 1)
+    ws = torch.empty(max(nb, 16), dtype=torch.uint8, device=dev) if nb else None
+
+    def step():
+        r = csa.index_fused_raw(p, q, k, w, qs, ks, st, idx, None, ws, stream)
+        if r != csa.CSA_OK:
+            raise RuntimeError(f"csa_index_fused returned {r}")
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    time.sleep(0.25)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if csa.device_status(stream) != csa.CSA_OK:
+        raise RuntimeError(f"device status word reports an error after {wl.name}")
+    ms = e0.elapsed_time(e1) / steps
+    peaks, peak_src = read_peaks()
+    out = {"workload": wl.name, "seed": wl.seed, "B": wl.B, "S": wl.S, "W": wl.W, "top_k": wl.top_k,
+           "steps": steps, "ms_per_step": ms, "value": wk["flops"] / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+           "rows_per_s": wk["rows"] / (ms * 1e-3), "nontrivial_rows": wk["nontrivial_rows"],
+           "tflops_nontrivial_rows": wk["flops_nontrivial"] / (ms * 1e-3) / 1e12, "clocks": clk}
+    if wl.name.startswith("decode"):
+        bytes_alg = decode_bytes(wl)
+        hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+        out["roofline"] = {"bound": "hbm", "achieved": bytes_alg / (ms * 1e-3) / 1e9, "peak": hbm, "unit": "GB/s",
+                           "frac": bytes_alg / (ms * 1e-3) / 1e9 / hbm, "traffic": measured_traffic(wl.name),
+                           "peak_source": f"{peak_src} hbm_gbs",
+                           "achieved_counts": "k + q + w bytes read, scores written and re-read, indices written "
+                                              "(score kernel + selection kernel per step)"}
+    else:
+        bf = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+        a = wk["flops_nontrivial"] / (ms * 1e-3) / 1e12
+        out["roofline"] = {"bound": "tensor", "achieved": a, "peak": bf, "unit": "TFLOP/s", "frac": a / bf,
+                           "traffic": None, "peak_source": f"{peak_src} bf16_tflops",
+                           "achieved_counts": "2*H*D per visible pair of rows with visible > top_k"}
+    del q, k, w, qs, ks, st, idx, ws
+    return out
+
+
+def decode_bytes(wl):
+    """Algorithmic bytes of one decode step: k, q and w read, the fp32 scores
+    written and read back by the selection, the indices written."""
+    return (wl.B * wl.W * wl.D * 2 + wl.B * wl.H * wl.S * wl.D * 2 + wl.B * wl.S * wl.H * 2
+            + 2 * wl.B * wl.S * wl.W * 4 + wl.B * wl.S * wl.top_k * 4)
 
 
 def backward_leg(wl, wk, q, k, w, q_seg, kv_seg, q_start, dev, stream, steps, warmup=3):
@@ -545,6 +650,8 @@ def main():
                     help="time the backward of the score step instead (its own JSON line)")
     ap.add_argument("--no-backward", action="store_true",
                     help="skip the backward measurement reported beside the forward")
+    ap.add_argument("--no-side", action="store_true",
+                    help="skip the decode and packed-document legs reported beside the headline")
     ap.add_argument("--gather", action="store_true",
                     help="also time the gather of the selected compressed rows (reported, not in the step)")
     args = ap.parse_args()

@@ -141,9 +141,12 @@ csa_status csa_index_gather(const csa_problem* p, const void* k, const int32_t* 
  *    e.g. 64 decode rows of 32768 entries).  Larger problems return
  *    CSA_ERR_UNSUPPORTED before anything is launched.  Every GPU that loads
  *    the library holds this array until the process exits.
- *  - The first call on a device looks up the array's device address (once,
- *    with that device current); make that first call before any stream
- *    capture in the calling program.
+ *  - The first call on a device looks up the array's device address (with
+ *    that device current) and keeps it; make that first call before any
+ *    stream capture in the calling program.  A failed lookup returns
+ *    CSA_ERR_CUDA and is tried again on the next call.  The kept address
+ *    belongs to the device's primary context: do not reset the device
+ *    (cudaDeviceReset) between calls.
  *  - All calls share the one array: calls whose work overlaps on the GPU
  *    (other streams, other host threads) race and corrupt each other's
  *    results.  Each call writes every score it later reads, so nothing needs

@@ -6,6 +6,7 @@
 #include <algorithm>
 #include <cmath>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 
 #include "csa_index.h"
@@ -225,25 +226,27 @@ size_t fused_workspace_bytes(const csa_problem* p) {
 constexpr size_t kNoAllocMaxScores = (size_t)2 * 1024 * 1024;
 static __device__ __align__(256) float g_noalloc_scores[kNoAllocMaxScores];
 
-// Device address of g_noalloc_scores on the current device, looked up once per
-// device (with that device current) and cached.
+// Device address of g_noalloc_scores on the current device, looked up with
+// that device current on the first successful call there and kept for later
+// calls.  A failed lookup is not kept: the next call tries again.  The
+// address stays valid for the life of the device's primary context.
 float* noalloc_scratch(cudaError_t* err) {
-  constexpr int kMaxDevices = 64;
-  static std::once_flag flags[kMaxDevices];
-  static float* ptrs[kMaxDevices];
-  static cudaError_t errs[kMaxDevices];
+  static std::atomic<float*> ptrs[kMaxDevices];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
     *err = cudaErrorInvalidDevice;
     return nullptr;
   }
-  std::call_once(flags[dev], [dev] {
-    void* ptr = nullptr;
-    errs[dev] = cudaGetSymbolAddress(&ptr, g_noalloc_scores);
-    ptrs[dev] = static_cast<float*>(ptr);
-  });
-  *err = errs[dev];
-  return errs[dev] == cudaSuccess ? ptrs[dev] : nullptr;
+  float* p = ptrs[dev].load(std::memory_order_acquire);
+  if (p != nullptr) {
+    *err = cudaSuccess;
+    return p;
+  }
+  void* ptr = nullptr;
+  *err = cudaGetSymbolAddress(&ptr, g_noalloc_scores);
+  if (*err != cudaSuccess) return nullptr;
+  ptrs[dev].store(static_cast<float*>(ptr), std::memory_order_release);
+  return static_cast<float*>(ptr);
 }
 
 }  // namespace

@@ -432,15 +432,8 @@ size_t backward_kernel_smem() { return kBSmem; }
 
 cudaError_t launch_backward_kernel(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tp,
                                    const BwdParams& bp, cudaStream_t stream) {
-  static int configured_device = -1;
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  cudaError_t e = smem_limit_once<csa_backward_kernel>((int)kBSmem);
   if (e != cudaSuccess) return e;
-  if (configured_device != dev) {
-    e = cudaFuncSetAttribute(csa_backward_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kBSmem);
-    if (e != cudaSuccess) return e;
-    configured_device = dev;
-  }
   if (bp.n_items <= 0) return cudaSuccess;
   const int grid = bp.grid < bp.n_items ? bp.grid : bp.n_items;
   csa_backward_kernel<<<grid, kBThreads, kBSmem, stream>>>(tq, tk, tp, bp);

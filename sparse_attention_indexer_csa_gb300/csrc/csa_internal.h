@@ -7,10 +7,33 @@
 #include <stdint.h>
 
 #include <algorithm>
+#include <atomic>
+#include <mutex>
 
 #include "csa_score_kernel.cuh"
 
 namespace csa {
+
+constexpr int kMaxDevices = 64;
+
+// Raises the dynamic shared-memory limit of kernel `Fn` to `bytes` on the
+// current device, once per device and thread-safe; a failed attempt is not
+// remembered, so a later call tries again.
+template <auto Fn>
+cudaError_t smem_limit_once(int bytes) {
+  static std::atomic<bool> done[kMaxDevices];
+  static std::mutex mu;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  if (done[dev].load(std::memory_order_acquire)) return cudaSuccess;
+  std::lock_guard<std::mutex> guard(mu);
+  if (done[dev].load(std::memory_order_relaxed)) return cudaSuccess;
+  e = cudaFuncSetAttribute(Fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done[dev].store(true, std::memory_order_release);
+  return e;
+}
 
 // Which instantiation of the persistent kernel to launch.
 struct KernelChoice {

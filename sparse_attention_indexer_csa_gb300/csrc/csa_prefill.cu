@@ -11,15 +11,8 @@ template <class C>
 cudaError_t launch_cfg(const CUtensorMap& tq, const CUtensorMap& tk, const KParams& p, int grid,
                        cudaStream_t stream) {
   const size_t smem = C::smem_bytes(p.w_pad);
-  static int configured_device = -1;  // attribute set once per device
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  cudaError_t e = smem_limit_once<csa_index_kernel<C>>(227 * 1024);
   if (e != cudaSuccess) return e;
-  if (configured_device != dev) {
-    e = cudaFuncSetAttribute(csa_index_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-    if (e != cudaSuccess) return e;
-    configured_device = dev;
-  }
   csa_index_kernel<C><<<grid, C::NTHREADS, smem, stream>>>(tq, tk, p);
   return cudaGetLastError();
 }

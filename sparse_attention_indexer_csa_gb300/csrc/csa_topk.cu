@@ -619,15 +619,8 @@ template <int NT>
 cudaError_t launch_topk_nt(const float* scores, int32_t* idx, long long rows, int W, int K, cudaStream_t stream) {
   // sized from the very layout the kernel instantiation uses
   const size_t smem = TopkCfg<NT>::smem(W);
-  static int configured_device = -1;
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  cudaError_t e = smem_limit_once<csa_topk_kernel<NT>>(227 * 1024);
   if (e != cudaSuccess) return e;
-  if (configured_device != dev) {
-    e = cudaFuncSetAttribute(csa_topk_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-    if (e != cudaSuccess) return e;
-    configured_device = dev;
-  }
   const long long grid = rows < 1048576 ? rows : 1048576;
   csa_topk_kernel<NT><<<(unsigned)grid, NT, smem, stream>>>(scores, idx, rows, W, K);
   return cudaGetLastError();
@@ -637,15 +630,8 @@ cudaError_t launch_topk_cluster(const float* scores, int32_t* idx, long long row
                                 cudaStream_t stream) {
   const int seg = (((W + kCl - 1) / kCl) + 127) & ~127;
   const size_t smem = kClHeader + (size_t)seg * sizeof(float);
-  static int configured_device = -1;
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  cudaError_t e = smem_limit_once<csa_topk_cluster_kernel>(227 * 1024);
   if (e != cudaSuccess) return e;
-  if (configured_device != dev) {
-    e = cudaFuncSetAttribute(csa_topk_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-    if (e != cudaSuccess) return e;
-    configured_device = dev;
-  }
   // one cluster per row; rows beyond one launch's grid go to further launches
   const long long per_launch = 65536;
   for (long long r0 = 0; r0 < rows; r0 += per_launch) {

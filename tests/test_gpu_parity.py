@@ -118,6 +118,32 @@ def test_full_size_prefill(name, seed):
         check_select_vs_oracle(ref, gi[b:b + 1, rows], wl.top_k)
 
 
+def test_full_size_fused_debug_scores():
+    """prefill_16k at B=1 through the fused kernel with its score copy: the
+    copy equals the score kernel's scores bit for bit, the oracle selector on
+    the copy gives the fused indices on every row, and asking for the copy
+    (which makes the kernel score its rows at or below top_k too) leaves the
+    indices unchanged."""
+    wl = WORKLOADS["prefill_16k"].with_(B=1, seed=3)
+    inp = make_inputs(wl)
+    d = to_dev(inp)
+    idx_dbg, dbg = gpu_fused(inp, d, dbg=True)
+    idx_p, _ = gpu_fused(inp, d, dbg=False)
+    gs = gpu_scores(inp, d)
+    assert_status_ok()
+    assert torch.equal(idx_dbg, idx_p)
+    assert torch.equal(dbg, gs)
+    del gs
+    g = dbg.cpu().numpy()
+    gi = idx_dbg.cpu().numpy()
+    del dbg
+    check_select_exact(g, gi, wl.top_k)
+    rows = _sample_rows(wl.S, wl.W, wl.compress_rate, wl.top_k, n=512, seed=5)
+    ref = oracle_scores(inp, rows=rows)
+    check_scores(g[:, rows], ref)
+    check_select_vs_oracle(ref, gi[:, rows], wl.top_k)
+
+
 def test_decode_full():
     wl = WORKLOADS["decode_32k"]
     inp = make_inputs(wl)

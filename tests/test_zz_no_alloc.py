@@ -15,6 +15,7 @@ import torch
 
 import sparse_attention_indexer_csa_gb300 as csa
 from csa_inputs import WORKLOADS, Workload, make_inputs
+from oracle import csa_oracle as O
 
 pytestmark = pytest.mark.gpu
 
@@ -50,6 +51,42 @@ def _two_calls_match_fused(inp):
 def test_decode_rows_match_fused():
     # 8 single-row sequences over 32768 entries: the decode-style path
     _two_calls_match_fused(make_inputs(WORKLOADS["decode_32k"].with_(B=8, seed=5)))
+
+
+def test_selection_equals_oracle_selector_on_gpu_scores():
+    # the oracle's selector, run on the scores of csa_index_score (the same
+    # score kernel the no-allocation path runs), reproduces its indices
+    wl = WORKLOADS["prefill_4k"].with_(S=700, W=175, top_k=50, seed=11)
+    inp = make_inputs(wl)
+    q, k, w, qs, ks, st = _dev(inp)
+    sc = csa.index_score(q, k, w, wl.scale, wl.compress_rate)
+    p = csa.make_problem(q, k, w, wl.scale, wl.compress_rate, wl.top_k)
+    out = torch.empty(wl.B, wl.S, wl.top_k, dtype=torch.int32, device="cuda")
+    assert csa.abi.index_fused_noalloc_raw(p, q, k, w, None, None, None, out) == csa.CSA_OK
+    torch.cuda.synchronize()
+    assert csa.device_status() == csa.CSA_OK
+    ref = O.select_topk(sc.double().cpu().numpy(), wl.top_k)
+    assert np.array_equal(out.cpu().numpy(), ref)
+
+
+def test_calls_ordered_on_a_non_default_stream():
+    # two calls enqueued on one side stream, the second right behind the
+    # first (the scratch is reused in stream order), read after that stream
+    wl = WORKLOADS["decode_32k"].with_(B=4, W=8192, q_start=32767, seed=12)
+    inp = make_inputs(wl)
+    q, k, w, qs, ks, st = _dev(inp)
+    ref = csa.index_fused(q, k, w, wl.scale, wl.compress_rate, wl.top_k, q_start=st)
+    torch.cuda.synchronize()
+    p = csa.make_problem(q, k, w, wl.scale, wl.compress_rate, wl.top_k)
+    side = torch.cuda.Stream()
+    outs = [torch.full((wl.B, wl.S, wl.top_k), -7, dtype=torch.int32, device="cuda") for _ in range(2)]
+    side.wait_stream(torch.cuda.current_stream())
+    for o in outs:
+        assert csa.abi.index_fused_noalloc_raw(p, q, k, w, None, None, st, o, stream=side) == csa.CSA_OK
+    side.synchronize()
+    assert csa.device_status(side) == csa.CSA_OK
+    for o in outs:
+        assert torch.equal(o, ref)
 
 
 def test_prefill_rows_match_fused():
