@@ -597,8 +597,8 @@ def backward_leg(wl, wk, q, k, w, q_seg, kv_seg, q_start, dev, stream, steps, wa
 
 def run_backward(args, wl, inp):
     """One line for the backward of the score step (csa_index_backward):
-    dq, dk, dw for a fixed seeded cotangent of the scores; per step the
-    chunked P kernel, the chunk copies of q and the cuBLAS GEMMs."""
+    dq, dk, dw for a fixed seeded cotangent of the scores; per step a memset
+    of dk, the dq/dw kernel and the dk kernel."""
     import sparse_attention_indexer_csa_gb300 as csa
 
     if not torch.cuda.is_available():
@@ -628,8 +628,8 @@ def run_backward(args, wl, inp):
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": None,
                      "peak_source": f"{peak_src} ({'MEASURED_PEAKS.json' if peak_src == 'measured' else 'recipe fallback'})",
-                     "achieved_counts": "3 x 2*H*D per visible pair (logits recomputed, dq, dk); the whole step, "
-                                        "several kernels and library GEMMs"},
+                     "achieved_counts": "3 x 2*H*D per visible pair (logits recomputed, dq, dk); the whole step: "
+                                        "the dq/dw kernel and the dk kernel (each recomputes the logits)"},
         "e2e": None, "gpu_launches": None, "clocks": clk,
     }
     print(json.dumps(line), flush=True)

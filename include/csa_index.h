@@ -158,28 +158,25 @@ csa_status csa_index_fused_noalloc(const csa_problem* p, const void* q, const vo
 /* Backward of the score step: the gradients of sum(g * score) over the
  * visible entries, for a cotangent g of the scores ("Add StreamIndex Kernel
  * for CSA [Deepseek v4]", Description: the custom_vjp whose backward is the
- * autodiff of the reference computation).  With x = q[b,h,s,:].k[b,t,:] and
- * gm = g on visible entries, 0 on masked ones (masked scores are constants):
+ * autodiff of the reference computation; its backward review asks for a
+ * fused kernel).  With x = q[b,h,s,:].k[b,t,:] and gm = g on visible
+ * entries, 0 on masked ones (masked scores are constants):
  *   dw[b,s,h] = sum_t gm * ReLU(scale * x)
  *   P         = gm * w[b,s,h] * scale * [x > 0]
  *   dq[b,h,s,:] = sum_t P * k[b,t,:],   dk[b,t,:] = sum_{h,s} P * q[b,h,s,:].
  * Inputs as for csa_index_score; g [B,S,W] fp32 (values at masked entries
  * are ignored); writes dq in q's layout ([B,H,S,D] or [B,S,H,D], q_layout),
- * dk [B,W,D] and dw [B,S,H], all fp32, every element.  Needs `workspace`:
- * csa_index_workspace_size(p, 2) bytes (256-byte aligned), which holds P for
- * one chunk of up to 8192 query rows ([rows, H, W] bf16, at most 4 GiB;
- * fewer rows when W is large) and, for head-major q, the chunk's q rows in
- * the same (row, head) order: the [B,H,S,W] tensor is never formed.  Per
- * chunk: a tensor-core kernel forms P and dw, then two library GEMMs per
- * sub-block of 2048 rows (cuBLAS, fp32 accumulation) form dq and add the
- * sub-block's share of dk; without q_start each sub-block's P and GEMMs span
- * only the entries its last row sees.  P is rounded to
- * bf16 before the GEMMs; dw is accumulated in fp32 from fp32 products.
- * Several kernels and GEMMs run on `stream` per chunk; the call returns once
- * they are enqueued.  The first call on a device creates the library's
- * cuBLAS handle for that device (cuBLAS allocates its own workspace then);
- * later calls allocate nothing.  Supported: H = 64, D = 128, either q layout.
- * Added in ABI version 102.                                              */
+ * dk [B,W,D] and dw [B,S,H], all fp32, every element; dq and dk need
+ * 16-byte aligned bases.  Two tensor-core kernels recompute the logits tile
+ * by tile and keep P (rounded to bf16) on the SM: one forms dw and dq per
+ * pair of query rows, the other dk per tile of 128 entries and run of row
+ * pairs, adding its partial sums into dk with fp32 atomics (so the last bits
+ * of dk may differ from call to call); the [B,H,S,W] tensor and P never
+ * reach HBM.  Needs `workspace`: csa_index_workspace_size(p, 2) bytes
+ * (256; 16-byte aligned), a work counter the call resets.  dk is zeroed and
+ * two kernels run on `stream`; the call returns once they are enqueued and
+ * allocates nothing.  Supported: H = 64, D = 128, either q layout.
+ * Added in ABI version 102; the workspace shrank to 256 bytes in 103.     */
 csa_status csa_index_backward(const csa_problem* p, const void* q, const void* k, const void* w,
                               const int32_t* q_seg, const int32_t* kv_seg, const int64_t* q_start,
                               const float* g, float* dq, float* dk, float* dw, void* workspace,

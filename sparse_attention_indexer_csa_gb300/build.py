@@ -2,8 +2,7 @@
 
 Each translation unit under ``csrc/`` is compiled by nvcc in parallel and the
 objects are linked into one shared library with the CUDA runtime linked
-statically; at run time it needs the NVIDIA driver and the toolkit's cuBLAS
-(the backward's two GEMMs), located through the library's rpath.
+statically; at run time it needs only the NVIDIA driver.
 """
 from __future__ import annotations
 
@@ -26,15 +25,6 @@ def nvcc() -> str:
     if not os.path.exists(cand):
         raise RuntimeError("nvcc not found: the CUDA toolkit is required to build libcsa_index.so")
     return cand
-
-
-def cuda_lib_dir(cc: str) -> str:
-    """Library directory of the toolkit that owns `cc` (for cuBLAS)."""
-    root = os.path.dirname(os.path.dirname(os.path.realpath(cc)))
-    for cand in (os.path.join(root, "lib64"), os.path.join(root, "lib")):
-        if os.path.exists(os.path.join(cand, "libcublas.so")):
-            return cand
-    return os.path.join(root, "lib64")
 
 
 def _flags(extra):
@@ -67,10 +57,7 @@ def build(verbose: bool = False, extra_flags=()) -> str:
         msg = "\n".join(f"--- {s}\n{t}" for s, t in failed)
         raise RuntimeError(f"nvcc failed:\n{msg}")
     tmp = LIB + ".tmp"
-    libdir = cuda_lib_dir(cc)
-    # the backward's dq / dk GEMMs use cuBLAS, found at run time through the rpath
-    link = [cc] + ARCH + ["-shared", "-o", tmp] + objs + ["-cudart", "static", "-L", libdir, "-lcublas",
-                                                       "-Xlinker", "-rpath", "-Xlinker", libdir]
+    link = [cc] + ARCH + ["-shared", "-o", tmp] + objs + ["-cudart", "static"]
     res = subprocess.run(link, stdout=subprocess.PIPE, stderr=subprocess.STDOUT)
     if res.returncode != 0:
         raise RuntimeError("link failed:\n" + res.stdout.decode(errors="replace"))

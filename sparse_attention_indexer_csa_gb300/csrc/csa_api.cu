@@ -129,46 +129,21 @@ bool make_k_map(CUtensorMap* m, const csa_problem* p, const void* k) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Chunk buffer of the backward: P [rows, H, w_pad] bf16 as dims (w_pad, H, rows);
-// box {64, 32, 1} = 64 entries of one row for 32 heads, stored from one
-// epilogue warp's 128-byte-swizzled staging tile.
-bool make_p_map(CUtensorMap* m, const void* pbuf, int rows, int w_pad, int H) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[3] = {(cuuint64_t)w_pad, (cuuint64_t)H, (cuuint64_t)rows};
-  cuuint64_t strides[2] = {(cuuint64_t)w_pad * 2, (cuuint64_t)H * w_pad * 2};
-  cuuint32_t box[3] = {64, 32, 1};
-  cuuint32_t estr[3] = {1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(pbuf), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-// Backward chunking.  A chunk is one launch of the P kernel; its P stays in
-// the workspace for the chunk's GEMMs.  Each GEMM sub-block of a chunk spans
-// only the entries its own last row sees, so the padding of P to a common
-// range is bounded by the sub-block, not the chunk.  At S = 16384, W = 4096
-// (timed on one GB300): sub-blocks of 2048 rows beat 256, 512, 1024 and 4096
-// (smaller ones give smaller, less efficient GEMMs; larger ones more padding),
-// and chunks of 8192 rows beat 2048 and 4096 (fewer launches, the pairs of
-// rows spread more evenly over the CTAs).
-constexpr int kBwdSubRows = 2048;
-constexpr int kBwdChunkRowsMax = 8192;
-constexpr size_t kBwdPBytesMax = (size_t)4 << 30;  // P's share of the workspace at most
-
-int bwd_chunk_rows(const csa_problem* p) {
-  const size_t per_row = (size_t)p->H * w_pad_of(p) * 2;  // bytes of P per query row
-  long long rc = std::min(p->S, kBwdChunkRowsMax);
-  rc = std::min<long long>(rc, std::max<long long>(2, (long long)(kBwdPBytesMax / per_row)));
-  return (int)((rc + 1) & ~1ll);
-}
-size_t round256(size_t x) { return (x + 255) & ~(size_t)255; }
-size_t bwd_p_bytes(const csa_problem* p) {
-  return round256((size_t)p->H * bwd_chunk_rows(p) * w_pad_of(p) * 2);
-}
+// Backward workspace: the dk kernel's item counter.
+constexpr size_t kBwdWorkspace = 256;
 size_t backward_workspace_bytes(const csa_problem* p) {
   if (check_problem(p) != CSA_OK) return 0;
-  return bwd_p_bytes(p) + round256((size_t)p->H * bwd_chunk_rows(p) * p->D * 2);
+  return kBwdWorkspace;
+}
+
+// Row pairs per dk item: 256, halved while the problem would give fewer than
+// about eight items per SM before the causal half is skipped (down to 32).
+int bwd_chunk_pairs(const csa_problem* p, int sms) {
+  const long long n_pairs = (p->S + 1) / 2;
+  const long long n_tiles = (p->W + kTileT - 1) / kTileT;
+  int cp = 256;
+  while (cp > 32 && (long long)p->B * n_tiles * ((n_pairs + cp - 1) / cp) < 8ll * sms) cp /= 2;
+  return cp;
 }
 
 csa_status run_index_kernel(const csa_problem* p, bool fused, const void* q, const void* k, const void* w,
@@ -349,107 +324,42 @@ csa_status csa_index_backward(const csa_problem* p, const void* q, const void* k
   if (st != CSA_OK) return st;
   if ((st = check_inputs(p, q, k, w, q_seg, kv_seg, q_start)) != CSA_OK) return st;
   if (g == nullptr || dq == nullptr || dk == nullptr || dw == nullptr) return CSA_ERR_INVALID_ARG;
-  if (!aligned(g, 4) || !aligned(dq, 4) || !aligned(dk, 4) || !aligned(dw, 4)) return CSA_ERR_INVALID_ARG;
+  if (!aligned(g, 4) || !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dw, 4)) return CSA_ERR_INVALID_ARG;
   if (p->H != 64 || p->D != 128) return CSA_ERR_UNSUPPORTED;
-  const bool seq_major = p->q_layout == CSA_Q_SEQ_MAJOR;
-  const size_t need = backward_workspace_bytes(p);
-  if (workspace == nullptr || workspace_bytes < need || !aligned(workspace, 256)) return CSA_ERR_INVALID_ARG;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const int rc = bwd_chunk_rows(p), w_pad = w_pad_of(p);
-  uint8_t* pbuf = static_cast<uint8_t*>(workspace);
-  uint8_t* qcbuf = pbuf + bwd_p_bytes(p);
+  if (workspace == nullptr || workspace_bytes < backward_workspace_bytes(p) || !aligned(workspace, 16))
+    return CSA_ERR_INVALID_ARG;
+  const long long n_pairs = (p->S + 1) / 2;
+  if ((long long)p->B * n_pairs > 0x7FFFFFFFll) return CSA_ERR_UNSUPPORTED;
+  const int sms = num_sms();
+  if (sms <= 0) return CSA_ERR_CUDA;
   CUtensorMap tq, tk;
   if (!make_q_map(&tq, p, q, 2) || !make_k_map(&tk, p, k)) return CSA_ERR_CUDA;
-  // dk accumulates over chunks; dq rows and dw are written once each
-  if (cudaMemsetAsync(dk, 0, (size_t)p->B * p->W * p->D * sizeof(float), s) != cudaSuccess) return CSA_ERR_CUDA;
-  const size_t qrow = (size_t)p->D * 2;  // bytes of one q row
-  for (int b = 0; b < p->B; ++b) {
-    for (int s0 = 0; s0 < p->S; s0 += rc) {
-      const int rows = std::min(rc, p->S - s0);
-      // GEMM range: entries below the chunk's largest visible threshold (the
-      // last row's), or all entries when a per-sequence offset is given (its
-      // value lives on the device)
-      const int w_eff = q_start ? p->W : std::min<long long>(p->W, ((long long)s0 + rows) / p->compress_rate);
-      // dq in q's layout: [B,H,S,D] (rows D apart, heads S*D) or [B,S,H,D] (rows H*D, heads D)
-      float* dq_chunk = seq_major ? dq + ((size_t)b * p->S + s0) * p->H * p->D
-                                  : dq + ((size_t)b * p->H * p->S + s0) * p->D;
-      float* dw_chunk = dw + ((size_t)b * p->S + s0) * p->H;
-      if (w_eff == 0) {  // no visible entry in the chunk
-        const cudaError_t e1 =
-            seq_major ? cudaMemsetAsync(dq_chunk, 0, (size_t)rows * p->H * p->D * sizeof(float), s)
-                      : cudaMemset2DAsync(dq_chunk, (size_t)p->S * p->D * sizeof(float), 0,
-                                          (size_t)rows * p->D * sizeof(float), p->H, s);
-        if (e1 != cudaSuccess || cudaMemsetAsync(dw_chunk, 0, (size_t)rows * p->H * sizeof(float), s) != cudaSuccess)
-          return CSA_ERR_CUDA;
-        continue;
-      }
-      CUtensorMap tp;
-      if (!make_p_map(&tp, pbuf, rows, w_pad, p->H)) return CSA_ERR_CUDA;
-      // sub-blocks only where the host knows the thresholds (no per-sequence offsets)
-      const int sub = q_start ? 0 : kBwdSubRows;
-      BwdParams bp;
-      std::memset(&bp, 0, sizeof(bp));
-      bp.B = p->B;
-      bp.S = p->S;
-      bp.W = p->W;
-      bp.r = p->compress_rate;
-      bp.b = b;
-      bp.s_base = s0;
-      bp.rows = rows;
-      bp.n_items = (rows + 1) / 2;
-      bp.grid = num_sms();
-      if (bp.grid <= 0) return CSA_ERR_CUDA;
-      bp.T_eff = (w_eff + kTileT - 1) / kTileT;
-      bp.sub_rows = sub;
-      bp.w_f32 = (p->w_dtype == CSA_F32) ? 1 : 0;
-      bp.scale = p->scale;
-      bp.w = w;
-      bp.q_seg = q_seg;
-      bp.kv_seg = kv_seg;
-      bp.q_start = q_start;
-      bp.g = g;
-      bp.dw = dw;
-      // the chunk's q rows in P's (row, head) order: sequence-major q already
-      // is; for head-major q the kernel copies them into the workspace
-      bp.q_gather = seq_major ? nullptr : q;
-      bp.qc = seq_major ? nullptr : qcbuf;
-      bp.wait_ns = kWaitNs;
-      if (launch_backward_kernel(tq, tk, tp, bp, s) != cudaSuccess) return CSA_ERR_CUDA;
-      const uint8_t* qrows = seq_major ? static_cast<const uint8_t*>(q) + ((size_t)b * p->S + s0) * p->H * qrow
-                                       : static_cast<const uint8_t*>(qcbuf);
-      const int dq_row_stride = seq_major ? p->H * p->D : p->D;
-      const int step = sub > 0 ? sub : rows;
-      for (int r0 = 0; r0 < rows; r0 += step) {
-        const int rows_i = std::min(step, rows - r0);
-        // the same range as pair_tiles() gives the sub-block's pairs
-        const int w_i = sub > 0 ? (int)std::min<long long>(p->W, ((long long)s0 + r0 + rows_i) / p->compress_rate)
-                                : w_eff;
-        float* dq_i = dq_chunk + (size_t)r0 * dq_row_stride;
-        if (w_i == 0) {  // no visible entry in the sub-block: P was not written, dq is zero
-          const cudaError_t e1 =
-              seq_major ? cudaMemsetAsync(dq_i, 0, (size_t)rows_i * p->H * p->D * sizeof(float), s)
-                        : cudaMemset2DAsync(dq_i, (size_t)p->S * p->D * sizeof(float), 0,
-                                            (size_t)rows_i * p->D * sizeof(float), p->H, s);
-          if (e1 != cudaSuccess) return CSA_ERR_CUDA;
-          continue;
-        }
-        BwdGemms gm;
-        gm.H = p->H;
-        gm.D = p->D;
-        gm.rows = rows_i;
-        gm.w_eff = w_i;
-        gm.w_pad = w_pad;
-        gm.p = pbuf + (size_t)r0 * p->H * w_pad * 2;
-        gm.k = static_cast<const uint8_t*>(k) + (size_t)b * p->W * qrow;
-        gm.qc = qrows + (size_t)r0 * p->H * qrow;
-        gm.dq = dq_i;
-        gm.dq_head_stride = seq_major ? (long long)p->D : (long long)p->S * p->D;
-        gm.dq_row_stride = dq_row_stride;
-        gm.dk = dk + (size_t)b * p->W * p->D;
-        if (!backward_gemms(gm, s)) return CSA_ERR_CUDA;
-      }
-    }
-  }
+  BwdParams bp;
+  std::memset(&bp, 0, sizeof(bp));
+  bp.B = p->B;
+  bp.S = p->S;
+  bp.W = p->W;
+  bp.r = p->compress_rate;
+  bp.n_pairs = (int)n_pairs;
+  bp.n_items = (int)((long long)p->B * n_pairs);
+  bp.n_tiles = (p->W + kTileT - 1) / kTileT;
+  bp.chunk_pairs = bwd_chunk_pairs(p, sms);
+  bp.n_chunks = (int)((n_pairs + bp.chunk_pairs - 1) / bp.chunk_pairs);
+  if ((long long)p->B * bp.n_chunks * bp.n_tiles > 0x7FFFFFFFll) return CSA_ERR_UNSUPPORTED;
+  bp.w_f32 = (p->w_dtype == CSA_F32) ? 1 : 0;
+  bp.scale = p->scale;
+  bp.w = w;
+  bp.q_seg = q_seg;
+  bp.kv_seg = kv_seg;
+  bp.q_start = q_start;
+  bp.g = g;
+  bp.dq = dq;
+  bp.dq_seq_major = p->q_layout == CSA_Q_SEQ_MAJOR ? 1 : 0;
+  bp.dk = dk;
+  bp.dw = dw;
+  bp.counter = static_cast<unsigned int*>(workspace);
+  bp.wait_ns = kWaitNs;
+  if (launch_backward(tq, tk, bp, sms, static_cast<cudaStream_t>(stream)) != cudaSuccess) return CSA_ERR_CUDA;
   return CSA_OK;
 }
 
@@ -501,6 +411,6 @@ const char* csa_status_string(csa_status s) {
   return "unknown status";
 }
 
-int32_t csa_index_abi_version(void) { return 102; }
+int32_t csa_index_abi_version(void) { return 103; }
 
 }  // extern "C"

@@ -1,319 +1,361 @@
-// csa_backward.cu -- backward of the score step for one chunk of query rows,
-// and the two library GEMMs that finish it.
+// csa_backward.cu -- backward of the score step on the tensor cores: two
+// persistent kernels, no intermediate tensor in HBM.
 //
 // The score of "Add StreamIndex Kernel for CSA [Deepseek v4]" (Description) is
 //   score[b,s,t] = sum_h w[b,s,h] * ReLU(scale * x),  x = q[b,h,s,:] . k[b,t,:];
 // the page's custom_vjp takes the cotangent g[b,s,t] of the scores back to
 //   dw[b,s,h] = sum_t gm * ReLU(scale * x)
-//   P[b,h,s,t] = gm * w[b,s,h] * scale * [scale * x > 0]
+//   P[b,h,s,t] = gm * w[b,s,h] * scale * [x > 0]
 //   dq[b,h,s,:] = sum_t P * k[b,t,:]         dk[b,t,:] = sum_{h,s} P * q[b,h,s,:]
 // with gm = g on visible entries and 0 on masked ones (masked scores are
-// constants).  For a chunk of rows this kernel recomputes x on the tensor
-// cores, forms P in bf16 for the chunk only ([rows, H, W_pad] in the caller's
-// workspace -- never the whole [B,H,S,W]) and dw in registers; dq and dk are
-// then two plain GEMMs per sub-block of the chunk's rows (cuBLAS), each over
-// the entries the sub-block's last row sees -- the range of P a pair of rows
-// writes here.
+// constants), and a fused kernel is asked for in that page's backward review
+// (the reference vjp forms the [B,H,S,W] tensor).  Both kernels here
+// recompute the logits x tile by tile and keep P on the SM:
 //
-// Kernel layout (persistent: each CTA takes pairs of query rows in turn, 352
-// threads):
-//   warp 0  TMA: per pair the q block (2 rows x 64 heads x 128, as the UMMA A
-//           operand: M = 128 rows (row j, head h) -> 64 j + h), then its k
-//           tiles (128 entries, the B operand, N = 128) into three stages;
-//   warp 1  TMEM owner and UMMA issuer: per k tile one 128x128x128 product
-//           into one of two 128-column accumulators;
-//   warps 2-9  epilogue: warp w reads TMEM lanes 32*(w%4) .. (rows (j, h))
-//           and one half of the tile's 128 entries (warps 2-5 the first,
-//           6-9 the second), so each thread owns one (row, head) and walks
-//           64 entries per tile: dw in a register (the halves added once per
-//           pair), P converted to bf16 into the warp's own 128-byte-swizzled
-//           staging tile (32 heads x 64 entries), which lane 0 writes out
-//           with a 3-D TMA store (box {64 entries, 32 heads, 1 row}); each
-//           warp double-buffers its staging, so the warps never wait for
-//           one another inside a tile.
-//   warp 10  for head-major q, copies the chunk's q rows into P's (row, head)
-//           order (the dk GEMMs' operand) while the other warps form P.
-// Tiles past the pair's visible range but inside its sub-block's GEMM range
-// are written as zeros without any product.
-#include <cublas_v2.h>
+//   csa_bwd_dq_kernel   item = a pair of query rows (2 rows x 64 heads = the
+//                       128 TMEM lanes), walking the k tiles the pair sees:
+//                         X  = Q . K^T                 (A = q block, B = k tile, smem)
+//                         P  = gm * w * scale * [X > 0] in bf16, written back
+//                              over X in tensor memory; dw += gm * X
+//                         dQ += P . K                  (A = P in TMEM, B = k tile read MN-major)
+//                       dQ stays in TMEM until the pair's last tile, then goes
+//                       to dq once (fp32, q's layout).
+//   csa_bwd_dk_kernel   item = one k tile (the 128 TMEM lanes are its entries)
+//                       and a run of row pairs that see it:
+//                         X^T = K . Q^T                (A = k tile, B = q block)
+//                         P^T in bf16 over X^T in tensor memory
+//                         dK += P^T . Q                (A = P^T in TMEM, B = q block read MN-major)
+//                       each item's dK is added into dk with vector atomics;
+//                       items are handed out through a counter in the
+//                       caller's workspace.
+//
+// Tensor memory (512 columns): three 128-column logit buffers (X / P), so the
+// products of tile n+1 run while the epilogue forms P of tile n and the
+// product with P of tile n-1 is still queued, and one 128-column accumulator
+// (dQ or dK).  P overwrites the first 32 columns of each 64-column half of
+// its logit buffer (64 bf16 in 32 columns), which that half's warp has
+// already read, so no warp writes columns another warp still reads.
+//
+// Warp roles (15 warps, both kernels):
+//   warp 0      TMA producer (dk: also takes items from the counter and
+//               publishes them to the other roles through a ring of slots)
+//   warp 1      TMEM owner and issuer of the logit products (one thread)
+//   warp 14     issuer of the accumulate products (one thread): the two
+//               issuers own different accumulators, so the waits and
+//               commits of one overlap the other's products on the pipe
+//   warps 2-9   epilogue: warp w reads TMEM lanes 32*(w%4).., half w/6 of
+//               each logit buffer (dq: entries 64*half.., dk: row `half` of
+//               the pair)
+//   warps 10-13 drain of the accumulator (lanes 32*(w%4)..)
+// Every mbarrier wait is bounded; a wait that gives up raises the CTA's
+// abort flag and records CSA_ERR_TIMEOUT, and the other roles stop waiting.
 #include <cuda_bf16.h>
-
-#include <mutex>
 
 #include "csa_internal.h"
 
 namespace csa {
-
 namespace {
 
-constexpr int kBH = 64, kBD = 128, kBR = 2;
-constexpr int kBM = kBR * kBH;                      // 128 (row, head) pairs: UMMA M
-constexpr int kBNKC = kBD / 64;                     // K chunks of 64 (128-byte swizzled rows)
-constexpr uint32_t kBQChunk = kBM * 128;            // 16 KB
-constexpr uint32_t kBQBytes = kBQChunk * kBNKC;     // 32 KB
-constexpr uint32_t kBKChunk = kTileT * 128;         // 16 KB
-constexpr uint32_t kBKBytes = kBKChunk * kBNKC;     // 32 KB
-constexpr int kBStages = 3;
-constexpr uint32_t kBPWarp = 32 * 128;              // 4 KB: one warp's 32 heads x 64 entries of bf16
-constexpr uint32_t kBIdesc = idesc_bf16_f32(kBM, kTileT);
-constexpr int kBEpiWarps = 8;
-constexpr int kBGatherWarp = 2 + kBEpiWarps;       // copies the chunk's head-major q rows
-constexpr int kBThreads = 64 + 32 * kBEpiWarps + 32;
-constexpr uint32_t kBTmemCols = 256;                // two 128-column accumulators
-constexpr uint32_t kBEpiBar = 2;                    // named barrier of the epilogue warps
+constexpr int kBH = 64, kBD = 128;
+constexpr uint32_t kChunk = 128 * 128;             // 16 KB: 128 rows x 64 bf16 (one half of D)
+constexpr uint32_t kBlk = 2 * kChunk;              // 32 KB: q block (2 rows x 64 heads) or k tile
+constexpr int kQBufDq = 2, kKStDq = 4;             // dq kernel: q blocks, k tile stages
+constexpr int kKtBufDk = 2, kQStDk = 4;            // dk kernel: k tiles, q block stages
+constexpr int kXBuf = 3;                           // logit / P buffers in TMEM
+constexpr uint32_t kAccCol = 384;                  // accumulator columns [384, 512)
+constexpr uint32_t kTmemCols = 512;
+constexpr int kThreads = 15 * 32;
+constexpr int kAccWarp = 14;  // issuer of the accumulate products
+constexpr int kEpiWarps = 8, kDrainWarps = 4;
+constexpr int kItemSlots = 4;
+constexpr uint32_t kIdescX = idesc_bf16_f32(128, 128);       // both operands K-major (K = D)
+constexpr uint32_t kIdescAcc = idesc_bf16_f32_bmn(128, 128);  // B read MN-major (N = D)
 
-constexpr uint32_t OFF_BQ = 0;
-constexpr uint32_t OFF_BK = OFF_BQ + kBQBytes;
-constexpr uint32_t OFF_BP = OFF_BK + kBStages * kBKBytes;
-constexpr uint32_t OFF_BG = OFF_BP + kBEpiWarps * 2 * kBPWarp;  // 8 warps x 64 fp32 cotangents
-constexpr uint32_t OFF_BDW = OFF_BG + kBEpiWarps * 64 * 4;       // 2 x 128 partial dw of the second half
-constexpr uint32_t OFF_BBAR = OFF_BDW + 2 * kBM * 4;             // 2 + 2*stages + 4 barriers
-constexpr uint32_t OFF_BMISC = OFF_BBAR + 16 * 8;
-constexpr uint32_t kBSmem = OFF_BMISC + 64 + 1024;         // + alignment slack
+// ----------------------------------------------------------------- shared layouts
+// dq kernel: q blocks | k stages | g staging (8 warps x 2 x 64 fp32) |
+//            dw exchange (2 x 128 fp32) | barriers | misc
+constexpr uint32_t DQ_OFF_Q = 0;
+constexpr uint32_t DQ_OFF_K = DQ_OFF_Q + kQBufDq * kBlk;
+constexpr uint32_t DQ_OFF_G = DQ_OFF_K + kKStDq * kBlk;
+constexpr uint32_t DQ_OFF_DW = DQ_OFF_G + kEpiWarps * 2 * 64 * 4;
+constexpr uint32_t DQ_OFF_BAR = DQ_OFF_DW + 2 * 128 * 4;
+constexpr int DQ_NBAR = 2 * kQBufDq + 2 * kKStDq + 3 * kXBuf + 3;
+constexpr uint32_t DQ_OFF_MISC = DQ_OFF_BAR + DQ_NBAR * 8;
+constexpr uint32_t kDqSmem = DQ_OFF_MISC + 16 + 1024;  // + alignment slack
 
-struct BSm {
-  uint8_t* base;
-  __device__ uint8_t* q() const { return base + OFF_BQ; }
-  __device__ uint8_t* k(int i) const { return base + OFF_BK + i * kBKBytes; }
-  __device__ uint8_t* pstage(int e, int i) const { return base + OFF_BP + (e * 2 + i) * kBPWarp; }
-  __device__ float* g(int e) const { return reinterpret_cast<float*>(base + OFF_BG) + e * 64; }
-  __device__ float* dwp(int i) const { return reinterpret_cast<float*>(base + OFF_BDW) + i * kBM; }
-  __device__ uint64_t* bar(int i) const { return reinterpret_cast<uint64_t*>(base + OFF_BBAR) + i; }
-  __device__ uint64_t* q_full() const { return bar(0); }
-  __device__ uint64_t* q_empty() const { return bar(1); }
-  __device__ uint64_t* k_full(int i) const { return bar(2 + i); }
-  __device__ uint64_t* k_empty(int i) const { return bar(2 + kBStages + i); }
-  __device__ uint64_t* acc_full(int i) const { return bar(2 + 2 * kBStages + i); }
-  __device__ uint64_t* acc_empty(int i) const { return bar(4 + 2 * kBStages + i); }
-  __device__ uint32_t* tmem_slot() const { return reinterpret_cast<uint32_t*>(base + OFF_BMISC); }
-  __device__ volatile uint32_t* abort_flag() const {
-    return reinterpret_cast<volatile uint32_t*>(base + OFF_BMISC + 4);
-  }
+// dk kernel: k tiles | q stages | w staging (8 warps x 2 x 64 fp32) |
+//            item slots | barriers | misc
+struct DkItem {
+  int b, tile, p_lo, p_hi;  // b < 0: no more items
+};
+constexpr uint32_t DK_OFF_KT = 0;
+constexpr uint32_t DK_OFF_Q = DK_OFF_KT + kKtBufDk * kBlk;
+constexpr uint32_t DK_OFF_W = DK_OFF_Q + kQStDk * kBlk;
+constexpr uint32_t DK_OFF_ITEM = DK_OFF_W + kEpiWarps * 2 * 64 * 4;
+constexpr uint32_t DK_OFF_BAR = DK_OFF_ITEM + kItemSlots * sizeof(DkItem);
+constexpr int DK_NBAR = 2 * kItemSlots + 2 * kKtBufDk + 2 * kQStDk + 3 * kXBuf + 3;
+constexpr uint32_t DK_OFF_MISC = DK_OFF_BAR + DK_NBAR * 8;
+constexpr uint32_t kDkSmem = DK_OFF_MISC + 16 + 1024;
+static_assert(kDqSmem <= 227u * 1024u && kDkSmem <= 227u * 1024u, "shared memory budget");
+
+// Barrier indices.
+struct DqBars {
+  static constexpr int q_full = 0, q_empty = q_full + kQBufDq, k_full = q_empty + kQBufDq,
+                       k_empty = k_full + kKStDq, x_full = k_empty + kKStDq, p_full = x_full + kXBuf,
+                       x_free = p_full + kXBuf, acc_full = x_free + kXBuf, acc_empty = acc_full + 1,
+                       done = acc_empty + 1;
+};
+struct DkBars {
+  static constexpr int item_full = 0, item_empty = item_full + kItemSlots, kt_full = item_empty + kItemSlots,
+                       kt_empty = kt_full + kKtBufDk, q_full = kt_empty + kKtBufDk, q_empty = q_full + kQStDk,
+                       x_full = q_empty + kQStDk, p_full = x_full + kXBuf, x_free = p_full + kXBuf,
+                       acc_full = x_free + kXBuf, acc_empty = acc_full + 1, done = acc_empty + 1;
 };
 
-// Visible-entry threshold of absolute row s (future mask): entries t < thr.
-__device__ __forceinline__ int row_threshold(const BwdParams& p, int s) {
+// ----------------------------------------------------------------- shared helpers
+// Visible-entry bound of row s of batch b (future mask): entries t < thr.
+__device__ __forceinline__ int row_thr(const BwdParams& p, int b, int s) {
   if (s >= p.S) return 0;
-  const long long qs0 = p.q_start ? (long long)p.q_start[p.b] : 0ll;
+  const long long qs0 = p.q_start ? (long long)p.q_start[b] : 0ll;
   long long tv = (qs0 + s + 1) / p.r;
   tv = tv < 0 ? 0 : (tv > p.W ? p.W : tv);
   return (int)tv;
 }
 
-// Tiles of P written for the pair whose first row is sl0 (relative): the GEMM
-// range of its sub-block of rows, the same expression the host uses for that
-// sub-block's GEMMs; the chunk's range without sub-blocks.
-__device__ __forceinline__ int pair_tiles(const BwdParams& p, int sl0) {
-  if (p.sub_rows <= 0) return p.T_eff;
-  const int end = min(p.rows, (sl0 / p.sub_rows + 1) * p.sub_rows);
-  long long tv = ((long long)p.s_base + end) / p.r;
-  tv = tv > p.W ? p.W : tv;
-  return (int)((tv + kTileT - 1) / kTileT);
+// Operand forms of the two products (M = 128, N = 128, eight K-steps of 16):
+//  * logits: A and B are 128-row blocks in shared memory, K-major over D in
+//    two 64-wide chunks of 128-byte swizzled rows (kChunk apart); K-step ks
+//    starts 32 bytes further into each row (chunk ks / 4).
+//  * accumulate: A is P in tensor memory as the epilogue leaves it -- K
+//    indices 0..63 in columns x_col + 0..31, 64..127 in columns x_col + 64..95,
+//    eight columns per K-step -- and B the 128-row block of the other operand
+//    read MN-major: K index k is row k of the block, D contiguous within a
+//    128-byte row (the two 64-wide chunks kChunk apart, 8-row groups 1024 B
+//    apart), K-step ks starting 2048 bytes further.
+// Descriptors are built once per buffer and advanced by the start-field
+// increment (bytes / 16) of these offsets.
+
+// Two fp32 to packed bf16 (lower index in the low half).
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&v);
 }
 
-// Pair number `pair` of the chunk: its first row (relative and absolute), the
-// visible thresholds of its two rows, the tiles of P it writes and the tiles
-// that need products.
-struct PairInfo {
-  int sl0, s0, thr0, thr1, T, t_hi;
+__device__ __forceinline__ void drain_waits(uint64_t* full_bars, int nbuf, uint32_t count, const WaitCtl& ctl) {
+  // the most recent use of each buffer has landed: no copy still writes
+  // shared memory when the CTA exits
+  volatile uint32_t dummy = 0;
+  const WaitCtl dctl{&dummy, ctl.limit_ns};
+  for (uint32_t i = 0; i < (uint32_t)nbuf && i < count; ++i) {
+    const uint32_t last = count - 1 - i;
+    mbar_wait(full_bars + (last % nbuf), (last / nbuf) & 1u, dctl);
+  }
+}
+
+// ======================================================================= dq
+// Item `it` of the dq kernel: batch and pair, the longest pairs (latest rows)
+// first so the static round-robin over the CTAs stays balanced.
+struct DqItem {
+  int b, s0, thr0, thr1, T;
 };
-__device__ __forceinline__ PairInfo pair_info(const BwdParams& p, int pair) {
-  PairInfo pi;
-  pi.sl0 = 2 * pair;
-  pi.s0 = p.s_base + pi.sl0;
-  pi.thr0 = row_threshold(p, pi.s0);
-  pi.thr1 = (pi.sl0 + 1 < p.rows) ? row_threshold(p, pi.s0 + 1) : 0;
-  pi.T = pair_tiles(p, pi.sl0);
-  pi.t_hi = min(pi.T, (max(pi.thr0, pi.thr1) + kTileT - 1) / kTileT);
-  return pi;
+__device__ __forceinline__ DqItem dq_item(const BwdParams& p, int it) {
+  DqItem d;
+  d.b = it % p.B;
+  const int pair = p.n_pairs - 1 - it / p.B;
+  d.s0 = 2 * pair;
+  d.thr0 = row_thr(p, d.b, d.s0);
+  d.thr1 = row_thr(p, d.b, d.s0 + 1);
+  d.T = (max(d.thr0, d.thr1) + kTileT - 1) / kTileT;
+  return d;
 }
 
-__global__ void __launch_bounds__(kBThreads, 1)
-    csa_backward_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
-                        const __grid_constant__ CUtensorMap tmap_p, const BwdParams p) {
+__global__ void __launch_bounds__(kThreads, 1)
+    csa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
+                      const BwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  const BSm sm{base};
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base + DQ_OFF_BAR);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + DQ_OFF_MISC);
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(base + DQ_OFF_MISC + 4);
   const int warp = threadIdx.x / 32;
   const uint32_t lane = lane_id();
+  using Bq = DqBars;
 
   if (threadIdx.x == 0) {
-    mbar_init(sm.q_full(), 1);
-    mbar_init(sm.q_empty(), 1);
-    for (int i = 0; i < kBStages; ++i) {
-      mbar_init(sm.k_full(i), 1);
-      mbar_init(sm.k_empty(i), 1);
+    for (int i = 0; i < kQBufDq; ++i) {
+      mbar_init(bars + Bq::q_full + i, 1);
+      mbar_init(bars + Bq::q_empty + i, 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(sm.acc_full(i), 1);
-      mbar_init(sm.acc_empty(i), kBEpiWarps);
+    for (int i = 0; i < kKStDq; ++i) {
+      mbar_init(bars + Bq::k_full + i, 1);
+      // released by the accumulate product alone: it starts only after the
+      // epilogue has read the tile's logits, so the logit product is done
+      mbar_init(bars + Bq::k_empty + i, 1);
     }
-    *sm.abort_flag() = 0u;
+    for (int i = 0; i < kXBuf; ++i) {
+      mbar_init(bars + Bq::x_full + i, 1);
+      mbar_init(bars + Bq::p_full + i, kEpiWarps);
+      mbar_init(bars + Bq::x_free + i, 1);
+    }
+    mbar_init(bars + Bq::acc_full, 1);
+    mbar_init(bars + Bq::acc_empty, kDrainWarps);
+    mbar_init(bars + Bq::done, 2);
+    *abort_flag = 0u;
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&tmap_q);
     prefetch_tmap(&tmap_k);
-    prefetch_tmap(&tmap_p);
   }
   if (warp == 1) {
-    tmem_alloc(sm.tmem_slot(), kBTmemCols);
+    tmem_alloc(tmem_slot, kTmemCols);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem_base = *sm.tmem_slot();
-  const WaitCtl ctl{sm.abort_flag(), p.wait_ns};
-  // pairs in reverse order (the longest rows, most tiles, first), strided over the CTAs
+  const uint32_t tmem = *tmem_slot;
+  const WaitCtl ctl{abort_flag, p.wait_ns};
 
   if (warp == 0) {
-    if (lane == 0) {
+    if (lane == 0) {  // ---------------------------------------------- TMA producer
       const uint64_t q_pol = l2_policy_evict_first(), k_pol = l2_policy_evict_last();
-      uint32_t qcount = 0, kcount = 0;
+      uint32_t qc = 0, kc = 0;
       for (int it = blockIdx.x; it < p.n_items; it += gridDim.x) {
-        const PairInfo pi = pair_info(p, p.n_items - 1 - it);
-        if (pi.t_hi == 0) continue;
-        if (!mbar_wait(sm.q_empty(), (qcount & 1u) ^ 1u, ctl)) break;
-        mbar_arrive_expect_tx(sm.q_full(), kBQBytes);
-#pragma unroll
-        for (int c = 0; c < kBNKC; ++c)
-          tma_load_4d_hint(sm.q() + c * kBQChunk, &tmap_q, sm.q_full(), c * 64, 0, pi.s0, p.b, q_pol);
-        ++qcount;
-        bool ok = true;
-        for (int tile = 0; tile < pi.t_hi; ++tile, ++kcount) {
-          const int st = kcount % kBStages;
-          if (!(ok = mbar_wait(sm.k_empty(st), ((kcount / kBStages) & 1u) ^ 1u, ctl))) break;
-          mbar_arrive_expect_tx(sm.k_full(st), kBKBytes);
-#pragma unroll
-          for (int c = 0; c < kBNKC; ++c)
-            tma_load_3d_hint(sm.k(st) + c * kBKChunk, &tmap_k, sm.k_full(st), c * 64, tile * kTileT, p.b, k_pol);
+        const DqItem d = dq_item(p, it);
+        if (d.T == 0) continue;
+        const int qb = qc % kQBufDq;
+        if (mbar_wait(bars + Bq::q_empty + qb, ((qc / kQBufDq) & 1u) ^ 1u, ctl)) {
+          uint8_t* dst = base + DQ_OFF_Q + qb * kBlk;
+          mbar_arrive_expect_tx(bars + Bq::q_full + qb, kBlk);
+          for (int c = 0; c < 2; ++c)
+            tma_load_4d_hint(dst + c * kChunk, &tmap_q, bars + Bq::q_full + qb, c * 64, 0, d.s0, d.b, q_pol);
         }
-        if (!ok) break;
+        ++qc;
+        for (int tile = 0; tile < d.T; ++tile, ++kc) {
+          const int st = kc % kKStDq;
+          if (mbar_wait(bars + Bq::k_empty + st, ((kc / kKStDq) & 1u) ^ 1u, ctl)) {
+            uint8_t* dst = base + DQ_OFF_K + st * kBlk;
+            mbar_arrive_expect_tx(bars + Bq::k_full + st, kBlk);
+            for (int c = 0; c < 2; ++c)
+              tma_load_3d_hint(dst + c * kChunk, &tmap_k, bars + Bq::k_full + st, c * 64, tile * kTileT, d.b, k_pol);
+          }
+        }
       }
-      // no copy may still be landing in shared memory when the CTA exits
-      volatile uint32_t dummy = 0;
-      const WaitCtl drain_ctl{&dummy, ctl.limit_ns};
-      for (uint32_t i = 0; i < (uint32_t)kBStages && i < kcount; ++i) {
-        const uint32_t last = kcount - 1 - i;
-        mbar_wait(sm.k_full(last % kBStages), (last / kBStages) & 1u, drain_ctl);
-      }
-      if (qcount > 0) mbar_wait(sm.q_full(), (qcount - 1) & 1u, drain_ctl);
+      drain_waits(bars + Bq::k_full, kKStDq, kc, ctl);
+      drain_waits(bars + Bq::q_full, kQBufDq, qc, ctl);
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      uint32_t qcount = 0, kcount = 0, acount = 0;
-      const uint32_t q_addr = smem_u32(sm.q());
+    if (lane == 0) {  // ------------------------------------- logits issuer
+      // Two threads issue the products: this one X = Q . K^T, warp kAccWarp
+      // the accumulate products.  Each keeps its loop short -- descriptors
+      // built once and advanced by constants, ring indices wrapping with
+      // explicit phase bits, barriers addressed directly -- and its waits
+      // and commits overlap the other's products on the tensor pipe.
+      const uint32_t bar0 = smem_u32(bars);
+      const uint64_t qd0 = smem_desc_kmajor(smem_u32(base + DQ_OFF_Q), 128);
+      const uint64_t kd0 = smem_desc_kmajor(smem_u32(base + DQ_OFF_K), 128);
+      uint32_t qb = 0, qph = 0, kst = 0, kph = 0, xb = 0, xph = 0, n = 0;
+      bool alive = true;
       for (int it = blockIdx.x; it < p.n_items; it += gridDim.x) {
-        const PairInfo pi = pair_info(p, p.n_items - 1 - it);
-        if (pi.t_hi == 0) continue;
-        const bool q_ok = mbar_wait(sm.q_full(), qcount & 1u, ctl);
-        tc_fence_after();
-        bool ok = q_ok;
-        for (int tile = 0; tile < pi.t_hi; ++tile, ++kcount, ++acount) {
-          const int st = kcount % kBStages, a = acount & 1;
-          const bool k_ok = ok && mbar_wait(sm.k_full(st), (kcount / kBStages) & 1u, ctl);
-          const bool a_ok = k_ok && mbar_wait(sm.acc_empty(a), ((acount >> 1) & 1u) ^ 1u, ctl);
+        const DqItem d = dq_item(p, it);
+        if (d.T == 0) continue;
+        alive = alive && mbar_wait_u32(bar0 + 8u * (Bq::q_full + qb), qph, ctl);
+        const uint64_t qd = qd0 + (uint64_t)(qb * (kBlk >> 4));
+        for (int tile = 0; tile < d.T; ++tile) {
+          alive = alive && mbar_wait_u32(bar0 + 8u * (Bq::k_full + kst), kph, ctl);
+          if (n >= (uint32_t)kXBuf) alive = alive && mbar_wait_u32(bar0 + 8u * (Bq::x_free + xb), xph ^ 1u, ctl);
           tc_fence_after();
-          ok = q_ok && k_ok && a_ok;
-          if (ok) {
-            const uint32_t k_addr = smem_u32(sm.k(st));
-            const uint32_t d_tmem = tmem_base + (uint32_t)(a * kTileT);
+          if (alive) {  // X = Q . K^T into logit buffer xb
+            const uint64_t kd = kd0 + (uint64_t)(kst * (kBlk >> 4));
+            const uint32_t xt = tmem + xb * 128u;
 #pragma unroll
-            for (int c = 0; c < kBNKC; ++c) {
-#pragma unroll
-              for (int kk = 0; kk < 4; ++kk) {
-                const uint64_t adesc = smem_desc_kmajor(q_addr + c * kBQChunk + kk * 32, 128);
-                const uint64_t bdesc = smem_desc_kmajor(k_addr + c * kBKChunk + kk * 32, 128);
-                umma_bf16(d_tmem, adesc, bdesc, kBIdesc, (c | kk) != 0 ? 1u : 0u);
-              }
+            for (int ks = 0; ks < 8; ++ks) {
+              const uint64_t o = (uint64_t)(((ks >> 2) * kChunk + (ks & 3) * 32) >> 4);
+              umma_bf16(xt, qd + o, kd + o, kIdescX, ks != 0 ? 1u : 0u);
             }
           }
-          umma_commit(sm.k_empty(st));
-          umma_commit(sm.acc_full(a));
-          if (!ok) break;
+          umma_commit_u32(bar0 + 8u * (Bq::x_full + xb));
+          if (tile == d.T - 1) umma_commit_u32(bar0 + 8u * (Bq::q_empty + qb));
+          ++n;
+          if (++kst == (uint32_t)kKStDq) {
+            kst = 0;
+            kph ^= 1u;
+          }
+          if (++xb == (uint32_t)kXBuf) {
+            xb = 0;
+            xph ^= 1u;
+          }
         }
-        umma_commit(sm.q_empty());  // the q block may be replaced once these products are done
-        ++qcount;
-        if (!ok) break;
+        if (++qb == (uint32_t)kQBufDq) {
+          qb = 0;
+          qph ^= 1u;
+        }
       }
+      // both issuers' products have completed before TMEM is released
+      umma_commit_u32(bar0 + 8u * Bq::done);
+      volatile uint32_t dummy = 0;
+      const WaitCtl dctl{&dummy, ctl.limit_ns};
+      mbar_wait(bars + Bq::done, 0u, dctl);
     }
-  } else if (warp < kBGatherWarp) {
-    // epilogue: thread = TMEM lane m = 32*quarter + lane = (row j, head h);
-    // warp half hf takes entries hf*64 .. hf*64+63 of every tile
+  } else if (warp < 2 + kEpiWarps) {  // ------------------------------ epilogue
     const int e = warp - 2;
-    const int hf = e >> 2;
     const int quarter = warp & 3;
-    const int m = quarter * 32 + (int)lane;
-    const int j = m >> 6, h = m & 63;  // row of the pair (warp-uniform), head
-    const int h0 = 32 * (quarter & 1);  // first head of this warp
+    const int hf = e >> 2;                      // half of the tile's entries
+    const int m = quarter * 32 + (int)lane;     // TMEM lane: (row j, head h)
+    const int j = m >> 6, h = m & 63;
     const bool segs = p.q_seg != nullptr;
-    const uint32_t t_lane = tmem_base + ((uint32_t)(quarter * 32) << 16);
-    float* gb = sm.g(e);
-    const uint64_t p_pol = l2_policy_evict_last();
-    uint32_t acount = 0, scount = 0, icount = 0;
-    bool ok = true;
-    for (int it = blockIdx.x; it < p.n_items; it += gridDim.x, ++icount) {
-      const PairInfo pi = pair_info(p, p.n_items - 1 - it);
-      const int s = pi.s0 + j;
-      const bool row_ok = (pi.sl0 + j < p.rows) && s < p.S;
-      const int thr = j ? pi.thr1 : pi.thr0;
-      const int seg = (segs && row_ok) ? p.q_seg[(size_t)p.b * p.S + s] : 0;
+    const uint32_t t_lane = tmem + ((uint32_t)(quarter * 32) << 16);
+    float* gbuf = reinterpret_cast<float*>(base + DQ_OFF_G) + e * 128;
+    float* dwx = reinterpret_cast<float*>(base + DQ_OFF_DW);
+    uint32_t n = 0, ic = 0;
+    for (int it = blockIdx.x; it < p.n_items; it += gridDim.x, ++ic) {
+      const DqItem d = dq_item(p, it);
+      const int s = d.s0 + j;
+      const bool row_ok = s < p.S;
+      const int thr = j ? d.thr1 : d.thr0;
+      const int seg = (segs && row_ok) ? p.q_seg[(size_t)d.b * p.S + s] : 0;
       float wc = 0.f;
       if (row_ok) {
-        const size_t off = ((size_t)p.b * p.S + s) * kBH + h;
+        const size_t off = ((size_t)d.b * p.S + s) * kBH + h;
         wc = (p.w_f32 ? reinterpret_cast<const float*>(p.w)[off]
                       : __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p.w)[off])) *
              p.scale;
       }
-      // dw / scale in four independent packed partial sums (eight floats)
-      float2 dwa[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
       const float2 wc2 = make_float2(wc, wc);
-      // masked cotangents of this warp's row and half for one tile (two per
-      // lane); the next tile's are loaded while the current tile is processed
+      float2 dwa[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+      // masked cotangents of row s for this warp's 64 entries of a tile (two per lane)
       auto load_g = [&](int tile) -> float2 {
-        const int t0 = tile * kTileT + hf * 64 + 2 * (int)lane;
         float gv[2];
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
-          const int t = t0 + u;
+          const int t = tile * kTileT + hf * 64 + 2 * (int)lane + u;
           bool vis = row_ok && t < thr;
-          if (vis && segs) vis = p.kv_seg[(size_t)p.b * p.W + t] == seg;
-          gv[u] = vis ? p.g[((size_t)p.b * p.S + s) * p.W + t] : 0.f;
+          if (vis && segs) vis = p.kv_seg[(size_t)d.b * p.W + t] == seg;
+          gv[u] = vis ? p.g[((size_t)d.b * p.S + s) * p.W + t] : 0.f;
         }
         return make_float2(gv[0], gv[1]);
       };
-      float2 g_next = (pi.T > 0) ? load_g(0) : make_float2(0.f, 0.f);
-      for (int tile = 0; tile < pi.T; ++tile, ++scount) {
+      float2 g_next = (d.T > 0) ? load_g(0) : make_float2(0.f, 0.f);
+      for (int tile = 0; tile < d.T; ++tile, ++n) {
+        const int xb = n % kXBuf;
+        float* gb = gbuf + (n & 1u) * 64;
         *reinterpret_cast<float2*>(gb + 2 * lane) = g_next;
-        if (tile + 1 < pi.T) g_next = load_g(tile + 1);
-        // this warp's staging buffer of two stores ago has been read
-        if (lane == 0) bulk_wait_group_read<1>();
         __syncwarp();
-        uint8_t* stg = sm.pstage(e, (int)(scount & 1u)) + lane * 128u;
-        const bool computed = tile < pi.t_hi;
-        const int a = acount & 1;
-        if (computed && ok) {
-          ok = mbar_wait(sm.acc_full(a), (acount >> 1) & 1u, ctl);
-          tc_fence_after();
-        }
-        const bool live = computed && ok;
-        float va[32], vb[32];
-        const uint32_t col0 = (uint32_t)(a * kTileT + hf * 64);
-        if (live) {
-          tmem_ld32_start(t_lane + col0, va);
+        if (tile + 1 < d.T) g_next = load_g(tile + 1);
+        const bool ok = mbar_wait(bars + Bq::x_full + xb, (n / kXBuf) & 1u, ctl);
+        tc_fence_after();
+        const uint32_t ta = t_lane + (uint32_t)xb * 128u + (uint32_t)hf * 64u;
+        if (ok) {
+          float va[32], vb[32];
+          tmem_ld32_start(ta, va);
           tmem_wait32(va);
-        }
+          tmem_ld32_start(ta + 32u, vb);
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {  // 32 entries per chunk
-          float(&cur)[32] = (c & 1) ? vb : va;
-          float(&nxt)[32] = (c & 1) ? va : vb;
-          uint32_t pk[16];
-          if (live) {
-            if (c == 0) tmem_ld32_start(t_lane + col0 + 32u, nxt);
-            // scale > 0: [scale*x > 0] = [x > 0].  gm = g * [x > 0] gives both
-            // P = gm * w * scale and the dw term gm * x = g * ReLU(x) (the
-            // scale of dw is applied once per pair)
+          for (int c = 0; c < 2; ++c) {
+            float(&cur)[32] = c ? vb : va;
+            if (c) tmem_wait32(vb);
+            uint32_t pk[16];
             const float4* g4 = reinterpret_cast<const float4*>(gb + c * 32);
 #pragma unroll
             for (int i4 = 0; i4 < 8; ++i4) {
@@ -323,79 +365,112 @@ __global__ void __launch_bounds__(kBThreads, 1)
                 const int i = 2 * i4 + i2;
                 const float2 x = make_float2(cur[2 * i], cur[2 * i + 1]);
                 const float2 gg = i2 ? make_float2(gq.z, gq.w) : make_float2(gq.x, gq.y);
+                // scale > 0: [scale*x > 0] = [x > 0]; gm * x = g * ReLU(x)
                 const float2 gm = fmul2(gg, make_float2(step_pos(x.x), step_pos(x.y)));
                 dwa[i & 3] = ffma2(gm, x, dwa[i & 3]);
                 const float2 pv = fmul2(gm, wc2);
-                const __nv_bfloat162 b2 = __floats2bfloat162_rn(pv.x, pv.y);
-                pk[i] = *reinterpret_cast<const uint32_t*>(&b2);
+                pk[i] = pack_bf16(pv.x, pv.y);
               }
             }
-          } else {
-#pragma unroll
-            for (int i = 0; i < 16; ++i) pk[i] = 0u;  // tile without products: P = 0
+            // entries 32c .. 32c+31 of this half -> columns 16c .. 16c+15
+            // (already read: columns 0..31 hold va)
+            tmem_st16(ta + 16u * (uint32_t)c, pk);
           }
-          // 32 entries = 64 bytes: 16-byte chunks 4c .. 4c+3 of the row
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            const uint32_t chunk = (uint32_t)(4 * c + q4);
-            const uint32_t pos = chunk ^ (lane & 7u);  // 128-byte swizzle (row = lane)
-            *reinterpret_cast<uint4*>(stg + pos * 16u) =
-                make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
-          }
-          if (live && c == 0) tmem_wait32(nxt);
+          tmem_wait_st();
         }
-        if (computed) {
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(sm.acc_empty(a));
-          ++acount;
-        }
-        fence_proxy_async_shared();
+        tc_fence_before();
         __syncwarp();
-        if (lane == 0 && pi.sl0 + j < p.rows) {
-          // evict_last: the dq and dk GEMMs that follow read P back, and the
-          // part of the chunk that stays in L2 is not read from DRAM again
-          tma_store_3d_hint(&tmap_p, sm.pstage(e, (int)(scount & 1u)), tile * kTileT + hf * 64, h0, pi.sl0 + j,
-                            p_pol);
-          bulk_commit_group();
-        }
-        __syncwarp();
+        if (lane == 0) mbar_arrive(bars + Bq::p_full + xb);
       }
-      // dw: the second half's partial sums join the first half's (buffers
-      // alternate by pair, so one barrier per pair suffices)
+      // dw: this half's sum joins the other half's (buffers alternate by item)
       const float dw_acc =
           (((dwa[0].x + dwa[0].y) + (dwa[1].x + dwa[1].y)) + ((dwa[2].x + dwa[2].y) + (dwa[3].x + dwa[3].y))) *
           p.scale;
-      float* dwp = sm.dwp((int)(icount & 1u));
-      if (hf == 1) dwp[m] = dw_acc;
-      named_bar_sync(kBEpiBar, 32 * kBEpiWarps);
-      if (hf == 0 && row_ok) p.dw[((size_t)p.b * p.S + s) * kBH + h] = dw_acc + dwp[m];
+      float* slot = dwx + (ic & 1u) * 128;
+      if (hf == 1) slot[m] = dw_acc;
+      named_bar_sync(1 + quarter, 64);
+      if (hf == 0 && row_ok) p.dw[((size_t)d.b * p.S + s) * kBH + h] = dw_acc + slot[m];
     }
-    if (lane == 0) bulk_wait_group_all();
-  } else if (p.qc != nullptr) {
-    // head-major q: the chunk's q rows in P's (row, head) order for the dk
-    // GEMMs, as plain 16-byte copies spread over the CTAs while the other
-    // warps form P (eight loads in flight per lane)
-    const uint4* src = static_cast<const uint4*>(p.q_gather);
-    uint4* dst = static_cast<uint4*>(p.qc);
-    const long long n = (long long)p.rows * kBH * 16;  // 16 x 16 bytes per row of 128 bf16
-    const long long stride = (long long)gridDim.x * 32;
-    constexpr int U = 8;
-    for (long long i0 = (long long)blockIdx.x * 32 + lane; i0 < n; i0 += stride * U) {
-      uint4 v[U];
+  } else if (warp == kAccWarp) {
+    if (lane == 0) {  // --------------------------------- accumulate issuer
+      // dQ (+)= P . K per tile: P in the tile's logit buffer, K read MN-major
+      const uint32_t bar0 = smem_u32(bars);
+      const uint64_t km0 = smem_desc_mn_sw128(smem_u32(base + DQ_OFF_K), kChunk, 1024u);
+      uint32_t kst = 0, xb = 0, xph = 0, ac = 0;
+      bool alive = true;
+      for (int it = blockIdx.x; it < p.n_items; it += gridDim.x) {
+        const DqItem d = dq_item(p, it);
+        if (d.T == 0) continue;
+        for (int tile = 0; tile < d.T; ++tile) {
+          if (tile == 0) alive = alive && mbar_wait_u32(bar0 + 8u * Bq::acc_empty, (ac & 1u) ^ 1u, ctl);
+          alive = alive && mbar_wait_u32(bar0 + 8u * (Bq::p_full + xb), xph, ctl);
+          tc_fence_after();
+          if (alive) {
+            const uint32_t xa = tmem + xb * 128u;
+            const uint64_t bd = km0 + (uint64_t)(kst * (kBlk >> 4));
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const long long i = i0 + u * stride;
-        if (i < n) {
-          const long long rh = i >> 4;
-          const int r = (int)(rh / kBH), hh = (int)(rh % kBH);
-          v[u] = src[(((size_t)p.b * kBH + hh) * p.S + p.s_base + r) * 16 + (i & 15)];
+            for (int ks = 0; ks < 8; ++ks) {
+              umma_bf16_tmem_a(tmem + kAccCol, xa + 64u * (uint32_t)(ks >> 2) + 8u * (uint32_t)(ks & 3),
+                               bd + (uint64_t)(128 * ks), kIdescAcc, (tile != 0 || ks != 0) ? 1u : 0u);
+            }
+          }
+          umma_commit_u32(bar0 + 8u * (Bq::k_empty + kst));
+          umma_commit_u32(bar0 + 8u * (Bq::x_free + xb));
+          if (tile == d.T - 1) {
+            umma_commit_u32(bar0 + 8u * Bq::acc_full);
+            ++ac;
+          }
+          if (++kst == (uint32_t)kKStDq) kst = 0;
+          if (++xb == (uint32_t)kXBuf) {
+            xb = 0;
+            xph ^= 1u;
+          }
         }
       }
+      umma_commit_u32(bar0 + 8u * Bq::done);
+    }
+  } else {  // ---------------------------------------------------------- dQ drain
+    const int quarter = warp & 3;
+    const int m = quarter * 32 + (int)lane;
+    const int j = m >> 6, h = m & 63;
+    const uint32_t t_acc = tmem + ((uint32_t)(quarter * 32) << 16) + kAccCol;
+    uint32_t ac = 0;
+    for (int it = blockIdx.x; it < p.n_items; it += gridDim.x) {
+      const DqItem d = dq_item(p, it);
+      const int s = d.s0 + j;
+      const bool row_ok = s < p.S;
+      float* dst = p.dq + (p.dq_seq_major ? (((size_t)d.b * p.S + s) * kBH + h) * kBD
+                                          : (((size_t)d.b * kBH + h) * p.S + s) * kBD);
+      float4* d4 = reinterpret_cast<float4*>(dst);
+      if (d.T == 0) {  // no visible entry: dq rows are zero
+        if (row_ok)
+          for (int i = 0; i < kBD / 4; ++i) d4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        continue;
+      }
+      const bool ok = mbar_wait(bars + Bq::acc_full, ac & 1u, ctl);
+      tc_fence_after();
+      ++ac;
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const long long i = i0 + u * stride;
-        if (i < n) dst[i] = v[u];
+      for (int half = 0; half < 2; ++half) {
+        float va[32], vb[32];
+        if (ok) {
+          tmem_ld32_start(t_acc + 64u * half, va);
+          tmem_ld32_start(t_acc + 64u * half + 32u, vb);
+          tmem_wait32(va);
+          tmem_wait32(vb);
+        }
+        if (half == 1) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bars + Bq::acc_empty);
+        }
+        if (ok && row_ok) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) d4[16 * half + i] = make_float4(va[4 * i], va[4 * i + 1], va[4 * i + 2], va[4 * i + 3]);
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            d4[16 * half + 8 + i] = make_float4(vb[4 * i], vb[4 * i + 1], vb[4 * i + 2], vb[4 * i + 3]);
+        }
       }
     }
   }
@@ -403,67 +478,380 @@ __global__ void __launch_bounds__(kBThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem_base, kBTmemCols);
+  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
-// One cuBLAS handle per device, created on first use.  Setting its stream
-// and enqueueing the GEMMs happen under the device's mutex, so calls from
-// several host threads on one device do not race on the handle's stream.
-struct BlasSlot {
-  cublasHandle_t handle = nullptr;
-  std::mutex lock;
-};
-BlasSlot* blas_slot() {
-  static BlasSlot slots[64];
-  static std::once_flag flags[64];
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  std::call_once(flags[dev], [dev] {
-    cublasHandle_t h = nullptr;
-    if (cublasCreate(&h) != CUBLAS_STATUS_SUCCESS) h = nullptr;
-    slots[dev].handle = h;
-  });
-  return slots[dev].handle ? &slots[dev] : nullptr;
+// ======================================================================= dk
+// First pair of batch b that sees tile `tile`: the pair holding the first row
+// s with (q_start + s + 1) / r > 128 * tile; n_pairs if none.
+__device__ __forceinline__ int dk_first_pair(const BwdParams& p, int b, int tile) {
+  const long long qs0 = p.q_start ? (long long)p.q_start[b] : 0ll;
+  long long s_first = (long long)p.r * ((long long)tile * kTileT + 1) - qs0 - 1;
+  if (s_first < 0) s_first = 0;
+  if (s_first >= p.S) return p.n_pairs;
+  return (int)(s_first / 2);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    csa_bwd_dk_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
+                      const BwdParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base + DK_OFF_BAR);
+  DkItem* slots = reinterpret_cast<DkItem*>(base + DK_OFF_ITEM);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + DK_OFF_MISC);
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(base + DK_OFF_MISC + 4);
+  const int warp = threadIdx.x / 32;
+  const uint32_t lane = lane_id();
+  using Bk = DkBars;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kItemSlots; ++i) {
+      mbar_init(bars + Bk::item_full + i, 1);
+      mbar_init(bars + Bk::item_empty + i, 2 + kEpiWarps + kDrainWarps);
+    }
+    for (int i = 0; i < kKtBufDk; ++i) {
+      mbar_init(bars + Bk::kt_full + i, 1);
+      mbar_init(bars + Bk::kt_empty + i, 1);
+    }
+    for (int i = 0; i < kQStDk; ++i) {
+      mbar_init(bars + Bk::q_full + i, 1);
+      // released by the accumulate product alone (see the dq kernel)
+      mbar_init(bars + Bk::q_empty + i, 1);
+    }
+    for (int i = 0; i < kXBuf; ++i) {
+      mbar_init(bars + Bk::x_full + i, 1);
+      mbar_init(bars + Bk::p_full + i, kEpiWarps);
+      mbar_init(bars + Bk::x_free + i, 1);
+    }
+    mbar_init(bars + Bk::acc_full, 1);
+    mbar_init(bars + Bk::acc_empty, kDrainWarps);
+    mbar_init(bars + Bk::done, 2);
+    *abort_flag = 0u;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmap_q);
+    prefetch_tmap(&tmap_k);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const WaitCtl ctl{abort_flag, p.wait_ns};
+
+  // Consumers read the item descriptors in order; false once there are no more.
+  auto next_item = [&](uint32_t ic, DkItem& out) -> bool {
+    const int slot = ic % kItemSlots;
+    const bool ok = mbar_wait(bars + Bk::item_full + slot, (ic / kItemSlots) & 1u, ctl);
+    out = slots[slot];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bars + Bk::item_empty + slot);
+    return ok && out.b >= 0;
+  };
+
+  if (warp == 0) {
+    if (lane == 0) {  // ------------------------------- scheduler + TMA producer
+      const uint64_t q_pol = l2_policy_evict_last(), k_pol = l2_policy_evict_last();
+      const long long n_raw = (long long)p.B * p.n_chunks * p.n_tiles;
+      uint32_t ic = 0, qc = 0;
+      // raw item x -> (b, chunk, tile), tile fastest: the items of one chunk
+      // of rows (the same q blocks) are taken one after another
+      unsigned int x = atomicAdd(p.counter, 1u);
+      while (!*abort_flag) {
+        DkItem d{-1, 0, 0, 0};
+        while ((long long)x < n_raw) {
+          const int tile = (int)(x % (unsigned)p.n_tiles);
+          const int rest = (int)(x / (unsigned)p.n_tiles);
+          const int chunk = rest % p.n_chunks, b = rest / p.n_chunks;
+          x = atomicAdd(p.counter, 1u);  // the next one, while this one is set up
+          const int lo = max(chunk * p.chunk_pairs, dk_first_pair(p, b, tile));
+          const int hi = min((chunk + 1) * p.chunk_pairs, p.n_pairs);
+          if (lo < hi) {
+            d = DkItem{b, tile, lo, hi};
+            break;
+          }
+        }
+        const int slot = ic % kItemSlots;
+        if (!mbar_wait(bars + Bk::item_empty + slot, ((ic / kItemSlots) & 1u) ^ 1u, ctl)) break;
+        slots[slot] = d;
+        mbar_arrive(bars + Bk::item_full + slot);
+        if (d.b < 0) break;
+        const int kb = ic % kKtBufDk;
+        if (mbar_wait(bars + Bk::kt_empty + kb, ((ic / kKtBufDk) & 1u) ^ 1u, ctl)) {
+          uint8_t* dst = base + DK_OFF_KT + kb * kBlk;
+          mbar_arrive_expect_tx(bars + Bk::kt_full + kb, kBlk);
+          for (int c = 0; c < 2; ++c)
+            tma_load_3d_hint(dst + c * kChunk, &tmap_k, bars + Bk::kt_full + kb, c * 64, d.tile * kTileT, d.b, k_pol);
+        }
+        ++ic;
+        for (int pr = d.p_lo; pr < d.p_hi; ++pr, ++qc) {
+          const int st = qc % kQStDk;
+          if (mbar_wait(bars + Bk::q_empty + st, ((qc / kQStDk) & 1u) ^ 1u, ctl)) {
+            uint8_t* dst = base + DK_OFF_Q + st * kBlk;
+            mbar_arrive_expect_tx(bars + Bk::q_full + st, kBlk);
+            for (int c = 0; c < 2; ++c)
+              tma_load_4d_hint(dst + c * kChunk, &tmap_q, bars + Bk::q_full + st, c * 64, 0, 2 * pr, d.b, q_pol);
+          }
+        }
+      }
+      drain_waits(bars + Bk::q_full, kQStDk, qc, ctl);
+      drain_waits(bars + Bk::kt_full, kKtBufDk, ic, ctl);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {  // ------------------------------------- logits issuer
+      const uint32_t bar0 = smem_u32(bars);
+      const uint64_t td0 = smem_desc_kmajor(smem_u32(base + DK_OFF_KT), 128);
+      const uint64_t qd0 = smem_desc_kmajor(smem_u32(base + DK_OFF_Q), 128);
+      uint32_t slot = 0, sph = 0, kb = 0, kbph = 0, qst = 0, qph = 0, xb = 0, xph = 0, n = 0;
+      bool alive = true;
+      while (true) {
+        const bool have = mbar_wait_u32(bar0 + 8u * (Bk::item_full + slot), sph, ctl);
+        const DkItem d = slots[slot];
+        mbar_arrive(bars + Bk::item_empty + slot);
+        if (++slot == (uint32_t)kItemSlots) {
+          slot = 0;
+          sph ^= 1u;
+        }
+        if (!have || d.b < 0) break;
+        alive = alive && mbar_wait_u32(bar0 + 8u * (Bk::kt_full + kb), kbph, ctl);
+        const uint64_t ad = td0 + (uint64_t)(kb * (kBlk >> 4));
+        for (int pr = d.p_lo; pr < d.p_hi; ++pr) {
+          alive = alive && mbar_wait_u32(bar0 + 8u * (Bk::q_full + qst), qph, ctl);
+          if (n >= (uint32_t)kXBuf) alive = alive && mbar_wait_u32(bar0 + 8u * (Bk::x_free + xb), xph ^ 1u, ctl);
+          tc_fence_after();
+          if (alive) {  // X^T = K . Q^T into logit buffer xb
+            const uint64_t bd = qd0 + (uint64_t)(qst * (kBlk >> 4));
+            const uint32_t xt = tmem + xb * 128u;
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+              const uint64_t o = (uint64_t)(((ks >> 2) * kChunk + (ks & 3) * 32) >> 4);
+              umma_bf16(xt, ad + o, bd + o, kIdescX, ks != 0 ? 1u : 0u);
+            }
+          }
+          umma_commit_u32(bar0 + 8u * (Bk::x_full + xb));
+          if (pr == d.p_hi - 1) umma_commit_u32(bar0 + 8u * (Bk::kt_empty + kb));
+          ++n;
+          if (++qst == (uint32_t)kQStDk) {
+            qst = 0;
+            qph ^= 1u;
+          }
+          if (++xb == (uint32_t)kXBuf) {
+            xb = 0;
+            xph ^= 1u;
+          }
+        }
+        if (++kb == (uint32_t)kKtBufDk) {
+          kb = 0;
+          kbph ^= 1u;
+        }
+      }
+      umma_commit_u32(bar0 + 8u * Bk::done);
+      volatile uint32_t dummy = 0;
+      const WaitCtl dctl{&dummy, ctl.limit_ns};
+      mbar_wait(bars + Bk::done, 0u, dctl);
+    }
+  } else if (warp < 2 + kEpiWarps) {  // ------------------------------ epilogue
+    const int e = warp - 2;
+    const int quarter = warp & 3;
+    const int jr = e >> 2;  // row of the pair whose 64 heads this warp takes
+    const bool segs = p.q_seg != nullptr;
+    const uint32_t t_lane = tmem + ((uint32_t)(quarter * 32) << 16);
+    float* wbuf = reinterpret_cast<float*>(base + DK_OFF_W) + e * 128;
+    uint32_t ic = 0, n = 0;
+    DkItem d;
+    while (next_item(ic, d)) {
+      ++ic;
+      const int t = d.tile * kTileT + quarter * 32 + (int)lane;  // this thread's entry
+      const bool t_ok = t < p.W;
+      const int kvs = (segs && t_ok) ? p.kv_seg[(size_t)d.b * p.W + t] : 0;
+      // masked cotangent of (row, t) and the row's weights times scale (two per lane)
+      auto load_row = [&](int pr, float& gm, float2& w2) {
+        const int s = 2 * pr + jr;
+        gm = 0.f;
+        w2 = make_float2(0.f, 0.f);
+        if (s < p.S) {
+          bool vis = t < row_thr(p, d.b, s);
+          if (vis && segs) vis = p.q_seg[(size_t)d.b * p.S + s] == kvs;
+          if (vis) gm = p.g[((size_t)d.b * p.S + s) * p.W + t];
+          const size_t off = ((size_t)d.b * p.S + s) * kBH + 2 * lane;
+          float w0, w1;
+          if (p.w_f32) {
+            w0 = reinterpret_cast<const float*>(p.w)[off];
+            w1 = reinterpret_cast<const float*>(p.w)[off + 1];
+          } else {
+            w0 = __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p.w)[off]);
+            w1 = __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p.w)[off + 1]);
+          }
+          w2 = make_float2(w0 * p.scale, w1 * p.scale);
+        }
+      };
+      float gm_next;
+      float2 w_next;
+      load_row(d.p_lo, gm_next, w_next);
+      for (int pr = d.p_lo; pr < d.p_hi; ++pr, ++n) {
+        const int xb = n % kXBuf;
+        const float gm = gm_next;
+        float* wb = wbuf + (n & 1u) * 64;
+        *reinterpret_cast<float2*>(wb + 2 * lane) = w_next;
+        __syncwarp();
+        if (pr + 1 < d.p_hi) load_row(pr + 1, gm_next, w_next);
+        const bool ok = mbar_wait(bars + Bk::x_full + xb, (n / kXBuf) & 1u, ctl);
+        tc_fence_after();
+        const uint32_t ta = t_lane + (uint32_t)xb * 128u + (uint32_t)jr * 64u;
+        if (ok) {
+          if (__any_sync(0xFFFFFFFFu, gm != 0.f)) {
+            float va[32], vb[32];
+            tmem_ld32_start(ta, va);
+            tmem_wait32(va);
+            tmem_ld32_start(ta + 32u, vb);
+            const float2 gm2 = make_float2(gm, gm);
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+              float(&cur)[32] = c ? vb : va;
+              if (c) tmem_wait32(vb);
+              uint32_t pk[16];
+              const float4* w4 = reinterpret_cast<const float4*>(wb + c * 32);
+#pragma unroll
+              for (int i4 = 0; i4 < 8; ++i4) {
+                const float4 wq = w4[i4];
+#pragma unroll
+                for (int i2 = 0; i2 < 2; ++i2) {
+                  const int i = 2 * i4 + i2;
+                  const float2 ww = i2 ? make_float2(wq.z, wq.w) : make_float2(wq.x, wq.y);
+                  const float2 st2 = make_float2(step_pos(cur[2 * i]), step_pos(cur[2 * i + 1]));
+                  const float2 pv = fmul2(fmul2(gm2, ww), st2);
+                  pk[i] = pack_bf16(pv.x, pv.y);
+                }
+              }
+              tmem_st16(ta + 16u * (uint32_t)c, pk);
+            }
+          } else {  // no visible entry in this warp's 32 x 64 block: P = 0
+            uint32_t zk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) zk[i] = 0u;
+            tmem_st16(ta, zk);
+            tmem_st16(ta + 16u, zk);
+          }
+          tmem_wait_st();
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bars + Bk::p_full + xb);
+      }
+    }
+  } else if (warp == kAccWarp) {
+    if (lane == 0) {  // --------------------------------- accumulate issuer
+      // dK (+)= P^T . Q per pair: P^T in the pair's logit buffer, Q read MN-major
+      const uint32_t bar0 = smem_u32(bars);
+      const uint64_t qm0 = smem_desc_mn_sw128(smem_u32(base + DK_OFF_Q), kChunk, 1024u);
+      uint32_t slot = 0, sph = 0, qst = 0, xb = 0, xph = 0, ac = 0;
+      bool alive = true;
+      while (true) {
+        const bool have = mbar_wait_u32(bar0 + 8u * (Bk::item_full + slot), sph, ctl);
+        const DkItem d = slots[slot];
+        mbar_arrive(bars + Bk::item_empty + slot);
+        if (++slot == (uint32_t)kItemSlots) {
+          slot = 0;
+          sph ^= 1u;
+        }
+        if (!have || d.b < 0) break;
+        for (int pr = d.p_lo; pr < d.p_hi; ++pr) {
+          if (pr == d.p_lo) alive = alive && mbar_wait_u32(bar0 + 8u * Bk::acc_empty, (ac & 1u) ^ 1u, ctl);
+          alive = alive && mbar_wait_u32(bar0 + 8u * (Bk::p_full + xb), xph, ctl);
+          tc_fence_after();
+          if (alive) {
+            const uint32_t xa = tmem + xb * 128u;
+            const uint64_t bd = qm0 + (uint64_t)(qst * (kBlk >> 4));
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks)
+              umma_bf16_tmem_a(tmem + kAccCol, xa + 64u * (uint32_t)(ks >> 2) + 8u * (uint32_t)(ks & 3),
+                               bd + (uint64_t)(128 * ks), kIdescAcc, (pr != d.p_lo || ks != 0) ? 1u : 0u);
+          }
+          umma_commit_u32(bar0 + 8u * (Bk::q_empty + qst));
+          umma_commit_u32(bar0 + 8u * (Bk::x_free + xb));
+          if (pr == d.p_hi - 1) {
+            umma_commit_u32(bar0 + 8u * Bk::acc_full);
+            ++ac;
+          }
+          if (++qst == (uint32_t)kQStDk) qst = 0;
+          if (++xb == (uint32_t)kXBuf) {
+            xb = 0;
+            xph ^= 1u;
+          }
+        }
+      }
+      umma_commit_u32(bar0 + 8u * Bk::done);
+    }
+  } else {  // ---------------------------------------------------------- dK drain
+    const int quarter = warp & 3;
+    const uint32_t t_acc = tmem + ((uint32_t)(quarter * 32) << 16) + kAccCol;
+    uint32_t ic = 0, ac = 0;
+    DkItem d;
+    while (next_item(ic, d)) {
+      ++ic;
+      const int t = d.tile * kTileT + quarter * 32 + (int)lane;
+      const bool ok = mbar_wait(bars + Bk::acc_full, ac & 1u, ctl);
+      tc_fence_after();
+      ++ac;
+      float* dst = p.dk + ((size_t)d.b * p.W + t) * kBD;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        float va[32], vb[32];
+        if (ok) {
+          tmem_ld32_start(t_acc + 64u * half, va);
+          tmem_ld32_start(t_acc + 64u * half + 32u, vb);
+          tmem_wait32(va);
+          tmem_wait32(vb);
+        }
+        if (half == 1) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bars + Bk::acc_empty);
+        }
+        if (ok && t < p.W) {
+          float* d0 = dst + 64 * half;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) red_add_f32x4(d0 + 4 * i, va[4 * i], va[4 * i + 1], va[4 * i + 2], va[4 * i + 3]);
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            red_add_f32x4(d0 + 32 + 4 * i, vb[4 * i], vb[4 * i + 1], vb[4 * i + 2], vb[4 * i + 3]);
+        }
+      }
+    }
+  }
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
 }  // namespace
 
-size_t backward_kernel_smem() { return kBSmem; }
+size_t backward_kernel_smem() { return kDqSmem > kDkSmem ? kDqSmem : kDkSmem; }
 
-cudaError_t launch_backward_kernel(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tp,
-                                   const BwdParams& bp, cudaStream_t stream) {
-  cudaError_t e = smem_limit_once<csa_backward_kernel>((int)kBSmem);
+cudaError_t launch_backward(const CUtensorMap& tq, const CUtensorMap& tk, const BwdParams& bp, int sms,
+                            cudaStream_t stream) {
+  cudaError_t e = smem_limit_once<csa_bwd_dq_kernel>((int)kDqSmem);
   if (e != cudaSuccess) return e;
-  if (bp.n_items <= 0) return cudaSuccess;
-  const int grid = bp.grid < bp.n_items ? bp.grid : bp.n_items;
-  csa_backward_kernel<<<grid, kBThreads, kBSmem, stream>>>(tq, tk, tp, bp);
+  e = smem_limit_once<csa_bwd_dk_kernel>((int)kDkSmem);
+  if (e != cudaSuccess) return e;
+  // dk accumulates the items' partial sums; the item counter starts at 0
+  e = cudaMemsetAsync(bp.dk, 0, (size_t)bp.B * bp.W * kBD * sizeof(float), stream);
+  if (e != cudaSuccess) return e;
+  e = cudaMemsetAsync(bp.counter, 0, sizeof(unsigned int), stream);
+  if (e != cudaSuccess) return e;
+  const int grid_dq = bp.n_items < sms ? bp.n_items : sms;
+  csa_bwd_dq_kernel<<<grid_dq, kThreads, kDqSmem, stream>>>(tq, tk, bp);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  csa_bwd_dk_kernel<<<sms, kThreads, kDkSmem, stream>>>(tq, tk, bp);
   return cudaGetLastError();
-}
-
-// dq rows of the chunk (one GEMM per head, batched) and the chunk's share of
-// dk (one GEMM over all heads and rows), fp32 accumulation of bf16 operands.
-// Row-major operands are passed to the column-major library transposed.
-bool backward_gemms(const BwdGemms& gm, cudaStream_t stream) {
-  BlasSlot* slot = blas_slot();
-  if (slot == nullptr) return false;
-  std::lock_guard<std::mutex> guard(slot->lock);
-  cublasHandle_t h = slot->handle;
-  if (cublasSetStream(h, stream) != CUBLAS_STATUS_SUCCESS) return false;
-  const float one = 1.f, zero = 0.f;
-  // dq[h][rows x D] = P[:, h][rows x W_eff] . k[W_eff x D]   (column-major: D x rows = k^T . P^T);
-  // the rows of head h are H * w_pad apart in P, the heads w_pad apart
-  if (cublasGemmStridedBatchedEx(h, CUBLAS_OP_N, CUBLAS_OP_N, gm.D, gm.rows, gm.w_eff, &one, gm.k, CUDA_R_16BF,
-                                 gm.D, 0, gm.p, CUDA_R_16BF, gm.H * gm.w_pad, (long long)gm.w_pad, &zero, gm.dq,
-                                 CUDA_R_32F, gm.dq_row_stride, gm.dq_head_stride, gm.H, CUBLAS_COMPUTE_32F,
-                                 CUBLAS_GEMM_DEFAULT) != CUBLAS_STATUS_SUCCESS)
-    return false;
-  // dk[W_eff x D] += P_all^T[W_eff x (rows H)] . Q[(rows H) x D]   (column-major: D x W_eff = Q^T . P_all),
-  // P_all and Q with their rows in the same (row, head) order
-  if (cublasGemmEx(h, CUBLAS_OP_N, CUBLAS_OP_T, gm.D, gm.w_eff, gm.H * gm.rows, &one, gm.qc, CUDA_R_16BF, gm.D,
-                   gm.p, CUDA_R_16BF, gm.w_pad, &one, gm.dk, CUDA_R_32F, gm.D, CUBLAS_COMPUTE_32F,
-                   CUBLAS_GEMM_DEFAULT) != CUBLAS_STATUS_SUCCESS)
-    return false;
-  return true;
 }
 
 cudaError_t take_status_backward(uint32_t* out, cudaStream_t stream) {

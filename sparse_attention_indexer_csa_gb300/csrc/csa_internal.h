@@ -57,18 +57,16 @@ cudaError_t launch_gather(const void* k, const int32_t* idx, void* out, long lon
                           int sms, cudaStream_t stream);
 cudaError_t take_status_gather(uint32_t* out, cudaStream_t stream);
 
-// Backward of the score step for one batch and one chunk of query rows
-// (csa_backward.cu): P in bf16 into the chunk buffer and dw, then two GEMMs.
+// Backward of the score step (csa_backward.cu): the dq / dw kernel over
+// pairs of query rows, then the dk kernel over (k tile, run of row pairs)
+// items handed out through `counter`.
 struct BwdParams {
   int B, S, W, r;
-  int b;        // batch of this launch
-  int s_base;   // first row of the chunk
-  int rows;     // rows in the chunk
-  int n_items;  // pairs of rows: (rows + 1) / 2
-  int grid;     // CTAs (persistent; at most n_items are launched)
-  int T_eff;    // tiles of the chunk's GEMM range: P is written for [0, T_eff*128)
-  int sub_rows; // > 0: rows of a GEMM sub-block (even); a pair's P spans its sub-block's
-                // range, ceil(min(W, (s_base + end of sub-block) / r) / 128) tiles
+  int n_pairs;      // pairs of query rows per batch: (S + 1) / 2
+  int n_items;      // dq kernel items: B * n_pairs
+  int n_tiles;      // k tiles of 128 entries: ceil(W / 128)
+  int chunk_pairs;  // dk kernel: row pairs per item at most
+  int n_chunks;     // dk kernel: ceil(n_pairs / chunk_pairs)
   int w_f32;
   float scale;
   const void* w;
@@ -76,26 +74,17 @@ struct BwdParams {
   const int32_t* kv_seg;
   const int64_t* q_start;
   const float* g;
-  float* dw;
-  const void* q_gather;  // head-major q [B,H,S,D] to copy into qc, or null
-  void* qc;              // the chunk's q rows in (row, head) order [rows, H, D], or null
+  float* dq;          // fp32 in q's layout
+  int dq_seq_major;   // dq [B,S,H,D] (1) or [B,H,S,D] (0)
+  float* dk;          // [B,W,D] fp32 (zeroed, then accumulated)
+  float* dw;          // [B,S,H] fp32
+  unsigned int* counter;  // dk item counter (device memory, zeroed before the launch)
   unsigned long long wait_ns;
 };
-struct BwdGemms {
-  int H, D, rows, w_eff, w_pad;  // rows and GEMM range of one sub-block of a chunk
-  const void* p;       // P rows of the sub-block: [rows, H, w_pad] bf16
-  const void* k;       // [W, D] bf16 of the batch
-  const void* qc;      // the sub-block's q rows in the same (row, head) order: [rows, H, D] bf16
-  float* dq;           // dq of the sub-block's first row, head 0
-  long long dq_head_stride;  // floats between heads (S*D head-major, D sequence-major)
-  int dq_row_stride;         // floats between rows (D head-major, H*D sequence-major)
-  float* dk;           // dk[b] [W, D]
-};
-cudaError_t launch_backward_kernel(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tp,
-                                   const BwdParams& bp, cudaStream_t stream);
+// Enqueues the whole backward on `stream` (two memsets, two kernels).
+cudaError_t launch_backward(const CUtensorMap& tq, const CUtensorMap& tk, const BwdParams& bp, int sms,
+                            cudaStream_t stream);
 size_t backward_kernel_smem();
-bool backward_gemms(const BwdGemms& gm, cudaStream_t stream);
-// qc[h][r][:] = q[b, s0 + r, h, :] for a sequence-major q (bf16, D = 128).
 cudaError_t take_status_backward(uint32_t* out, cudaStream_t stream);
 
 // Kernel that waits on a barrier nothing completes, bounded by `ns`.

@@ -39,7 +39,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_abi_version_and_strings(lib):
-    assert lib.csa_index_abi_version() == 102
+    assert lib.csa_index_abi_version() == 103
     for s in range(6):
         assert abi.status_string(s)
     assert abi.status_string(99) == "unknown status"
@@ -116,13 +116,9 @@ def _bwd(lib, p, g=FAKE, dq=FAKE, dk=FAKE, dw=FAKE, ws=FAKE, nbytes=1 << 40, q=F
 
 
 def test_backward_workspace_size():
-    # P of one chunk of rows ([rows, H, W_pad] bf16) + the chunk's q rows ([rows, H, D] bf16); a chunk
-    # is at most 8192 rows and its P at most 4 GiB
-    assert abi.workspace_size(_p(S=16, W=4), 2) == 64 * 16 * 128 * 2 + 64 * 16 * 128 * 2
-    assert abi.workspace_size(_p(S=16384, W=4096), 2) == 64 * 8192 * 4096 * 2 + 64 * 8192 * 128 * 2
-    assert abi.workspace_size(_p(S=5, W=300), 2) == 64 * 6 * 384 * 2 + 64 * 6 * 128 * 2  # rows rounded to pairs
-    # wide rows: 4 GiB / (64 heads x 32768 entries x 2 bytes) = 1024 rows per chunk
-    assert abi.workspace_size(_p(S=16384, W=32768), 2) == 64 * 1024 * 32768 * 2 + 64 * 1024 * 128 * 2
+    # the dk kernel's work counter only: P never leaves the SM
+    for kw in (dict(S=16, W=4), dict(S=16384, W=4096), dict(S=5, W=300), dict(S=16384, W=32768)):
+        assert abi.workspace_size(_p(**kw), 2) == 256
     assert abi.workspace_size(_p(B=0), 2) == 0
 
 
@@ -134,6 +130,9 @@ def test_backward_argument_checks(lib):
     need = abi.workspace_size(_p(), 2)
     assert _bwd(lib, _p(), ws=None) == abi.CSA_ERR_INVALID_ARG
     assert _bwd(lib, _p(), nbytes=need - 1) == abi.CSA_ERR_INVALID_ARG
-    assert _bwd(lib, _p(), ws=ctypes.c_void_p(0x10010)) == abi.CSA_ERR_INVALID_ARG
+    assert _bwd(lib, _p(), ws=ctypes.c_void_p(0x10004)) == abi.CSA_ERR_INVALID_ARG
+    # dq and dk take 16-byte vector stores and atomics
+    assert _bwd(lib, _p(), dq=ctypes.c_void_p(0x10008)) == abi.CSA_ERR_INVALID_ARG
+    assert _bwd(lib, _p(), dk=ctypes.c_void_p(0x10008)) == abi.CSA_ERR_INVALID_ARG
     # only H=64, D=128
     assert _bwd(lib, _p(H=4, D=32)) == abi.CSA_ERR_UNSUPPORTED
