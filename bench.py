@@ -10,9 +10,12 @@ Prints one JSON line (rank 0).  ``value`` is useful causal TFLOP/s,
 2*H*D*(visible (s,t) pairs) / time, with inputs resident in HBM; ``e2e`` is
 the same metric with the host<->device copies of each step's inputs and
 result inside the timed region.  Under torchrun every rank runs its own
-replica of the workload (rows and batches are independent; no collective on
-the data path), so scaling is weak and ``value`` sums all ranks' work over
-the slowest rank's time.  ``--impl reference`` times the CPU oracle instead.
+replica of the workload by default (rows and batches are independent; no
+collective on the data path), so scaling is weak and ``value`` sums all
+ranks' work over the slowest rank's time; with ``--shard rows`` the ranks
+split the query rows of one problem instead (strong scaling; the shards'
+indices are gathered and checked against one full call after the timed
+region).  ``--impl reference`` times the CPU oracle instead.
 """
 from __future__ import annotations
 
@@ -265,12 +268,18 @@ def run_reference(args, wl, inp):
     print(json.dumps(line), flush=True)
 
 
-def config_dict(wl, n_gpus):
+def config_dict(wl, n_gpus, shard="replicas"):
+    if n_gpus <= 1:
+        par = "single GPU"
+    elif shard == "rows":
+        par = f"row shards x{n_gpus} (one problem, rows balanced by visible entries)"
+    else:
+        par = f"replicas x{n_gpus}"
     return {"workload": wl.name, "B": wl.B, "S": wl.S, "W": wl.W, "H": wl.H, "D": wl.D,
             "compress_rate": wl.compress_rate, "top_k": wl.top_k, "w_dtype": wl.w_dtype,
             "q_start": wl.q_start, "docs": list(wl.docs) if wl.docs else None,
             "global_batch": wl.B * n_gpus, "seq_len": wl.S,
-            "parallelism": f"replicas x{n_gpus}" if n_gpus > 1 else "single GPU",
+            "parallelism": par,
             "l2": "no flush: inputs larger than L2 (q is {:.0f} MiB)".format(
                 wl.B * wl.H * wl.S * wl.D * 2 / 2**20)}
 
@@ -287,19 +296,33 @@ def run_ours(args, wl, inp):
     csa.load()
     stream = torch.cuda.current_stream(dev)
     wk = work(inp)
+    full_inp = inp
+    rows_mode = args.shard == "rows"
+    s0 = s1 = 0
+    if rows_mode:
+        # this rank's query rows of the one shared problem, positioned by q_start
+        from sparse_attention_indexer_csa_gb300.shard import row_shards
+
+        s0, s1 = row_shards(wl.S, wl.W, wl.compress_rate, world, wl.q_start or 0)[rank]
+        base = inp.q_start if inp.q_start is not None else torch.zeros(wl.B, dtype=torch.int64)
+        inp = Inputs(wl, inp.q[:, :, s0:s1].contiguous(), inp.k, inp.w[:, s0:s1].contiguous(),
+                     None if inp.q_seg is None else inp.q_seg[:, s0:s1].contiguous(), inp.kv_seg, base + s0)
 
     q, k, w = inp.q.to(dev), inp.k.to(dev), inp.w.to(dev)
     q_seg = None if inp.q_seg is None else inp.q_seg.to(dev)
     kv_seg = None if inp.kv_seg is None else inp.kv_seg.to(dev)
     q_start = None if inp.q_start is None else inp.q_start.to(dev)
+    S_local = q.shape[2]
     p = csa.make_problem(q, k, w, wl.scale, wl.compress_rate, wl.top_k)
-    idx = torch.empty(wl.B, wl.S, wl.top_k, dtype=torch.int32, device=dev)
+    idx = torch.empty(wl.B, S_local, wl.top_k, dtype=torch.int32, device=dev)
     ws_bytes = csa.workspace_size(p, 1)
     ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev) if ws_bytes else None
     # decode-style single rows and rows longer than 4096 take two kernels
     launches_per_step = 2 if (wl.S <= 2 or wl.W > 4096) else 1
 
     def step():
+        if S_local == 0:  # an empty row shard
+            return
         st = csa.index_fused_raw(p, q, k, w, q_seg, kv_seg, q_start, idx, None, ws, stream)
         if st != csa.CSA_OK:
             raise RuntimeError(f"csa_index_fused returned {st}")
@@ -406,8 +429,31 @@ def run_ours(args, wl, inp):
             raise RuntimeError("end-to-end result differs from the device-resident result")
         del sets
 
-    total_flops = sum_over_ranks(wk["flops"], dist)
-    total_rows = sum_over_ranks(wk["rows"], dist)
+    shard_check = None
+    if rows_mode and world > 1:
+        # every rank's rows (padded to the longest shard), compared on rank 0
+        # with one call over all rows, outside the timed region
+        from sparse_attention_indexer_csa_gb300.shard import row_shards
+
+        maxr = int(max_over_ranks(float(S_local), dist))
+        pad = torch.full((wl.B, maxr, wl.top_k), -2, dtype=torch.int32, device=dev)
+        pad[:, :S_local] = idx
+        parts = [torch.empty_like(pad) for _ in range(world)]
+        dist.all_gather(parts, pad)
+        if rank == 0:
+            shards = row_shards(wl.S, wl.W, wl.compress_rate, world, wl.q_start or 0)
+            got = torch.cat([parts[r][:, :e - b] for r, (b, e) in enumerate(shards)], dim=1)
+            g = lambda t: None if t is None else t.to(dev)  # noqa: E731
+            full = csa.index_fused(g(full_inp.q), g(full_inp.k), g(full_inp.w), wl.scale, wl.compress_rate,
+                                   wl.top_k, g(full_inp.q_seg), g(full_inp.kv_seg), g(full_inp.q_start))
+            if not torch.equal(got, full):
+                raise RuntimeError("row shards differ from one call over all rows")
+            shard_check = f"bit-identical to one call over all rows (shards {shards})"
+    if rows_mode:  # one problem split over the ranks: its work, once
+        total_flops, total_rows = wk["flops"], wk["rows"]
+    else:
+        total_flops = sum_over_ranks(wk["flops"], dist)
+        total_rows = sum_over_ranks(wk["rows"], dist)
     value = total_flops / (ms_step * 1e-3) / 1e12
     peaks, peak_src = read_peaks()
     avg_launch_ms = sum(launch_ms) / len(launch_ms)
@@ -424,9 +470,10 @@ def run_ours(args, wl, inp):
 
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "strong" if rows_mode else "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": config_dict(wl, world),
+        "config": config_dict(wl, world, "rows" if rows_mode else "replicas"),
         "rows_per_s": total_rows / (ms_step * 1e-3),
         "useful_pairs": wk["pairs"], "nontrivial_rows": wk["nontrivial_rows"],
         "tflops_nontrivial_rows": wk["flops_nontrivial"] / (ms_step * 1e-3) / 1e12,
@@ -441,9 +488,11 @@ def run_ours(args, wl, inp):
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
             "overlap": "two buffer sets: the next step's input copies and the previous step's result copy "
                        "overlap the current step's compute (three streams)"},
-        "gpu_launches": launches_per_step * args.steps,
+        "gpu_launches": (launches_per_step if S_local > 0 else 0) * args.steps,
         "clocks": clk,
     }
+    if shard_check is not None:
+        line["shard_check"] = shard_check
     if args.gather:  # gather of the selected rows, timed on its own over the same selection
         gout = torch.empty(wl.B, wl.S, wl.top_k, wl.D, dtype=torch.bfloat16, device=dev)
         for _ in range(3):
@@ -650,6 +699,9 @@ def main():
                     help="time the backward of the score step instead (its own JSON line)")
     ap.add_argument("--no-backward", action="store_true",
                     help="skip the backward measurement reported beside the forward")
+    ap.add_argument("--shard", default="replicas", choices=["replicas", "rows"],
+                    help="under torchrun: independent replicas per rank (weak scaling) or one problem whose "
+                         "query rows are split over the ranks (strong scaling)")
     ap.add_argument("--no-side", action="store_true",
                     help="skip the decode and packed-document legs reported beside the headline")
     ap.add_argument("--gather", action="store_true",
@@ -667,7 +719,8 @@ def main():
         inp = make_inputs(wl.with_(seed=wl.seed + rank))
         run_reference(args, wl, inp)
         return
-    inp = make_inputs(wl.with_(seed=wl.seed + rank))
+    # replicas draw their own inputs; row shards all cut the same problem
+    inp = make_inputs(wl.with_(seed=wl.seed + (rank if args.shard == "replicas" else 0)))
     if args.backward:
         run_backward(args, wl, inp)
         return

@@ -16,8 +16,9 @@
  *
  * Conventions shared by every entry point
  * ---------------------------------------
- *  - All tensor pointers are DEVICE pointers owned by the caller, contiguous
- *    row-major, with 16-byte aligned bases.  The library never allocates,
+ *  - All tensor pointers are DEVICE pointers owned by the caller, row-major
+ *    (contiguous unless csa_problem gives strides for q, k or w), with
+ *    16-byte aligned bases.  The library never allocates,
  *    frees or synchronises in these calls; work is enqueued on `stream`
  *    (a cudaStream_t passed as void*; NULL = the legacy default stream) on
  *    the current device.
@@ -70,6 +71,22 @@ typedef enum { CSA_Q_HEAD_MAJOR = 0, CSA_Q_SEQ_MAJOR = 1 } csa_q_layout;
  *   top_k  >= 1 (may exceed the visible count or W: -1 padding),
  *   w_dtype  storage type of the weights (csa_dtype),
  *   q_layout  csa_q_layout of q (added in ABI version 101).
+ * Strided inputs (added in ABI version 104): q, k and w may be views into
+ * larger buffers -- e.g. q sliced out of a [B,S,H',D] projection output,
+ * so no copy is needed before the call.  Their innermost dimension (D for
+ * q and k, H for w) must be contiguous; the other strides are given in
+ * elements, and 0 (the value a zero-initialised struct holds) means the
+ * contiguous layout:
+ *   q_stride_b, q_stride_h, q_stride_s  of q's batch, head and row
+ *       dimensions (default: from q_layout); with the 16-byte-aligned base
+ *       they must be multiples of 8 elements (16 bytes, the TMA rule);
+ *   k_stride_b, k_stride_w  of k's batch and entry dimensions (default
+ *       W*D and D; multiples of 8 elements);
+ *   w_stride_b, w_stride_s  of w's batch and row dimensions (default S*H
+ *       and H; any positive value).
+ * Outputs (scores, idx, dq, dk, dw, gathered rows) are always contiguous;
+ * dq follows q_layout.  A stride that breaks these rules returns
+ * CSA_ERR_INVALID_ARG.
  * A decode batch with sequences of different lengths shares one k buffer
  * [B,W,D] sized for the longest; q_start[b] (the row's position) bounds
  * each sequence's visible entries, so entries past a sequence's length are
@@ -81,6 +98,9 @@ typedef struct {
   int32_t top_k;
   int32_t w_dtype;
   int32_t q_layout;
+  int64_t q_stride_b, q_stride_h, q_stride_s;
+  int64_t k_stride_b, k_stride_w;
+  int64_t w_stride_b, w_stride_s;
 } csa_problem;
 
 /* Scores.  q [B,H,S,D] (or [B,S,H,D], q_layout) bf16, k [B,W,D] bf16, w [B,S,H] (w_dtype),
@@ -201,7 +221,7 @@ csa_status csa_index_selftest_timeout(uint32_t timeout_us, void* stream);
 /* Static string for a status code. */
 const char* csa_status_string(csa_status s);
 
-/* ABI version (major * 100 + minor). */
+/* ABI version (major * 100 + minor): 104 (strides in csa_problem). */
 int32_t csa_index_abi_version(void);
 
 #ifdef __cplusplus

@@ -42,13 +42,16 @@ class CsaError(RuntimeError):
 
 
 class Problem(ctypes.Structure):
-    """Mirror of ``csa_problem``."""
+    """Mirror of ``csa_problem`` (strides in elements; 0 = contiguous)."""
 
     _fields_ = [
         ("B", ctypes.c_int32), ("H", ctypes.c_int32), ("S", ctypes.c_int32),
         ("D", ctypes.c_int32), ("W", ctypes.c_int32), ("compress_rate", ctypes.c_int32),
         ("scale", ctypes.c_float), ("top_k", ctypes.c_int32), ("w_dtype", ctypes.c_int32),
         ("q_layout", ctypes.c_int32),
+        ("q_stride_b", ctypes.c_int64), ("q_stride_h", ctypes.c_int64), ("q_stride_s", ctypes.c_int64),
+        ("k_stride_b", ctypes.c_int64), ("k_stride_w", ctypes.c_int64),
+        ("w_stride_b", ctypes.c_int64), ("w_stride_s", ctypes.c_int64),
     ]
 
 
@@ -98,12 +101,18 @@ def _check(fn: str, status: int):
         raise CsaError(fn, status, status_string(status))
 
 
-def _ptr(t: Optional[torch.Tensor]):
+def _ptr(t: Optional[torch.Tensor], strided: bool = False):
+    """Device pointer of `t`.  Inputs whose strides the problem carries (q, k,
+    w) may be views with a contiguous innermost dimension; every other
+    tensor must be contiguous."""
     if t is None:
         return None
     if not t.is_cuda:
         raise ValueError("tensors passed to the library must live on the GPU")
-    if not t.is_contiguous():
+    if strided:
+        if t.dim() > 0 and t.stride(-1) != 1 and t.shape[-1] != 1:
+            raise ValueError("the innermost dimension of q, k and w must be contiguous")
+    elif not t.is_contiguous():
         raise ValueError("tensors passed to the library must be contiguous")
     return ctypes.c_void_p(t.data_ptr())
 
@@ -117,21 +126,30 @@ def _stream(stream) -> ctypes.c_void_p:
 
 def make_problem(q: torch.Tensor, k: torch.Tensor, w: torch.Tensor, scale: float, compress_rate: int,
                  top_k: int = 1, q_layout: int = CSA_Q_HEAD_MAJOR) -> Problem:
-    """Problem of q [B,H,S,D] (head-major) or q [B,S,H,D] (q_layout=CSA_Q_SEQ_MAJOR)."""
+    """Problem of q [B,H,S,D] (head-major) or q [B,S,H,D] (q_layout=CSA_Q_SEQ_MAJOR),
+    k [B,W,D], w [B,S,H]; the tensors' own strides are passed on, so views
+    (e.g. q sliced out of a wider projection output) need no copy."""
     if q_layout == CSA_Q_SEQ_MAJOR:
         B, S, H, D = q.shape
+        qb, qs, qh = q.stride(0), q.stride(1), q.stride(2)
     else:
         B, H, S, D = q.shape
+        qb, qh, qs = q.stride(0), q.stride(1), q.stride(2)
     W = k.shape[1]
     wd = {torch.bfloat16: CSA_BF16, torch.float32: CSA_F32}.get(w.dtype)
     if wd is None:
         raise ValueError("weights must be bf16 or fp32")
-    return Problem(B, H, S, D, W, int(compress_rate), float(scale), int(top_k), wd, int(q_layout))
+    # a dimension of extent 1 has no meaningful stride: leave the default
+    one = lambda n, st: 0 if n == 1 else int(st)  # noqa: E731
+    return Problem(B, H, S, D, W, int(compress_rate), float(scale), int(top_k), wd, int(q_layout),
+                   one(B, qb), one(H, qh), one(S, qs), one(B, k.stride(0)), one(W, k.stride(1)),
+                   one(B, w.stride(0)), one(S, w.stride(1)))
 
 
 # ----------------------------------------------------------------------------- raw C-ABI calls
 def index_score_raw(p: Problem, q, k, w, q_seg, kv_seg, q_start, scores, stream=None) -> int:
-    return load().csa_index_score(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(w), _ptr(q_seg), _ptr(kv_seg),
+    return load().csa_index_score(ctypes.byref(p), _ptr(q, True), _ptr(k, True), _ptr(w, True), _ptr(q_seg),
+                                  _ptr(kv_seg),
                                   _ptr(q_start), _ptr(scores), _stream(stream))
 
 
@@ -144,21 +162,24 @@ def index_topk_raw(p: Problem, scores, idx, workspace=None, stream=None) -> int:
 def index_fused_raw(p: Problem, q, k, w, q_seg, kv_seg, q_start, idx, scores_dbg=None, workspace=None,
                     stream=None) -> int:
     nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    return load().csa_index_fused(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(w), _ptr(q_seg), _ptr(kv_seg),
+    return load().csa_index_fused(ctypes.byref(p), _ptr(q, True), _ptr(k, True), _ptr(w, True), _ptr(q_seg),
+                                  _ptr(kv_seg),
                                   _ptr(q_start), _ptr(idx), _ptr(scores_dbg), _ptr(workspace), nbytes,
                                   _stream(stream))
 
 
 def index_fused_noalloc_raw(p: Problem, q, k, w, q_seg, kv_seg, q_start, idx, stream=None) -> int:
     """csa_index_fused_noalloc: no workspace, scores in the library's static scratch."""
-    return load().csa_index_fused_noalloc(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(w), _ptr(q_seg), _ptr(kv_seg),
+    return load().csa_index_fused_noalloc(ctypes.byref(p), _ptr(q, True), _ptr(k, True), _ptr(w, True),
+                                          _ptr(q_seg), _ptr(kv_seg),
                                           _ptr(q_start), _ptr(idx), _stream(stream))
 
 
 def index_backward_raw(p: Problem, q, k, w, q_seg, kv_seg, q_start, g, dq, dk, dw, workspace=None,
                        stream=None) -> int:
     nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    return load().csa_index_backward(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(w), _ptr(q_seg), _ptr(kv_seg),
+    return load().csa_index_backward(ctypes.byref(p), _ptr(q, True), _ptr(k, True), _ptr(w, True), _ptr(q_seg),
+                                     _ptr(kv_seg),
                                      _ptr(q_start), _ptr(g), _ptr(dq), _ptr(dk), _ptr(dw), _ptr(workspace), nbytes,
                                      _stream(stream))
 
@@ -230,9 +251,11 @@ def index_gather(k, idx, out=None, stream=None):
     B, W, D = k.shape
     _, S, K = idx.shape
     p = Problem(B, 1, S, D, W, 1, 1.0, int(K), CSA_BF16, CSA_Q_HEAD_MAJOR)
+    p.k_stride_b = 0 if B == 1 else k.stride(0)
+    p.k_stride_w = 0 if W == 1 else k.stride(1)
     if out is None:
         out = torch.empty(B, S, K, D, dtype=k.dtype, device=k.device)
-    _check("csa_index_gather", load().csa_index_gather(ctypes.byref(p), _ptr(k), _ptr(idx), _ptr(out),
+    _check("csa_index_gather", load().csa_index_gather(ctypes.byref(p), _ptr(k, True), _ptr(idx), _ptr(out),
                                                        _stream(stream)))
     return out
 

@@ -23,6 +23,30 @@ constexpr unsigned long long kWaitNs = 2000000000ull;  // 2 s per wait before gi
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// Element strides of the inputs, the problem's own or the contiguous
+// defaults (a zero field selects the default).
+struct Strides {
+  long long qb, qh, qs;  // q: batch, head, row
+  long long kb, kw;      // k: batch, entry
+  long long wb, ws;      // w: batch, row
+};
+Strides strides_of(const csa_problem* p) {
+  const bool sm = p->q_layout == CSA_Q_SEQ_MAJOR;
+  const long long D = p->D, H = p->H, S = p->S, W = p->W;
+  Strides t;
+  t.qb = p->q_stride_b ? p->q_stride_b : H * S * D;
+  t.qh = p->q_stride_h ? p->q_stride_h : (sm ? D : S * D);
+  t.qs = p->q_stride_s ? p->q_stride_s : (sm ? H * D : D);
+  t.kb = p->k_stride_b ? p->k_stride_b : W * D;
+  t.kw = p->k_stride_w ? p->k_stride_w : D;
+  t.wb = p->w_stride_b ? p->w_stride_b : S * H;
+  t.ws = p->w_stride_s ? p->w_stride_s : H;
+  return t;
+}
+
+// q and k strides feed TMA maps: multiples of 16 bytes (8 bf16) below 2^40 bytes.
+bool tma_stride_ok(long long s) { return s >= 0 && (s % 8) == 0 && s < (1ll << 38); }
+
 csa_status check_problem(const csa_problem* p) {
   if (p == nullptr) return CSA_ERR_INVALID_ARG;
   if (p->B < 1 || p->H < 1 || p->S < 1 || p->D < 1 || p->W < 1) return CSA_ERR_INVALID_ARG;
@@ -32,6 +56,10 @@ csa_status check_problem(const csa_problem* p) {
   if (p->q_layout != CSA_Q_HEAD_MAJOR && p->q_layout != CSA_Q_SEQ_MAJOR) return CSA_ERR_INVALID_ARG;
   const double rows = (double)p->B * (double)p->S;
   if (rows * (double)p->W > 4.0e18 || rows * (double)p->top_k > 4.0e18) return CSA_ERR_INVALID_ARG;
+  for (long long st : {p->q_stride_b, p->q_stride_h, p->q_stride_s, p->k_stride_b, p->k_stride_w})
+    if (!tma_stride_ok(st)) return CSA_ERR_INVALID_ARG;
+  if (p->w_stride_b < 0 || p->w_stride_s < 0 || p->w_stride_b > (1ll << 40) || p->w_stride_s > (1ll << 40))
+    return CSA_ERR_INVALID_ARG;
   return CSA_OK;
 }
 
@@ -95,17 +123,15 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // q viewed as dims (D, H, S, B) so one box {KC, H, R, 1} lands as R*H rows
-// ordered (row j, head h) -> j*H + h.  Head-major [B,H,S,D] and
-// sequence-major [B,S,H,D] differ only in the strides of H and S.
+// ordered (row j, head h) -> j*H + h.  Head-major [B,H,S,D], sequence-major
+// [B,S,H,D] and strided views differ only in the strides of H, S and B.
 bool make_q_map(CUtensorMap* m, const csa_problem* p, const void* q, int R) {
   auto fn = encode_fn();
   if (!fn) return false;
   const int KC = (p->D % 64 == 0) ? 64 : 32;
   cuuint64_t dims[4] = {(cuuint64_t)p->D, (cuuint64_t)p->H, (cuuint64_t)p->S, (cuuint64_t)p->B};
-  const cuuint64_t row = (cuuint64_t)p->D * 2;
-  const bool seq_major = p->q_layout == CSA_Q_SEQ_MAJOR;
-  cuuint64_t strides[3] = {seq_major ? row : (cuuint64_t)p->S * row, seq_major ? (cuuint64_t)p->H * row : row,
-                           (cuuint64_t)p->H * p->S * row};
+  const Strides st = strides_of(p);
+  cuuint64_t strides[3] = {(cuuint64_t)st.qh * 2, (cuuint64_t)st.qs * 2, (cuuint64_t)st.qb * 2};
   cuuint32_t box[4] = {(cuuint32_t)KC, (cuuint32_t)p->H, (cuuint32_t)R, 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
   const CUtensorMapSwizzle sw = (KC == 64) ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
@@ -120,7 +146,8 @@ bool make_k_map(CUtensorMap* m, const csa_problem* p, const void* k) {
   if (!fn) return false;
   const int KC = (p->D % 64 == 0) ? 64 : 32;
   cuuint64_t dims[3] = {(cuuint64_t)p->D, (cuuint64_t)p->W, (cuuint64_t)p->B};
-  cuuint64_t strides[2] = {(cuuint64_t)p->D * 2, (cuuint64_t)p->W * p->D * 2};
+  const Strides st = strides_of(p);
+  cuuint64_t strides[2] = {(cuuint64_t)st.kw * 2, (cuuint64_t)st.kb * 2};
   cuuint32_t box[3] = {(cuuint32_t)KC, (cuuint32_t)kTileT, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   const CUtensorMapSwizzle sw = (KC == 64) ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
@@ -163,6 +190,8 @@ csa_status run_index_kernel(const csa_problem* p, bool fused, const void* q, con
   kp.scale = p->scale;
   kp.w_f32 = (p->w_dtype == CSA_F32) ? 1 : 0;
   kp.w = w;
+  kp.w_sb = strides_of(p).wb;
+  kp.w_ss = strides_of(p).ws;
   kp.q_seg = q_seg;
   kp.kv_seg = kv_seg;
   kp.q_start = q_start;
@@ -349,6 +378,8 @@ csa_status csa_index_backward(const csa_problem* p, const void* q, const void* k
   bp.w_f32 = (p->w_dtype == CSA_F32) ? 1 : 0;
   bp.scale = p->scale;
   bp.w = w;
+  bp.w_sb = strides_of(p).wb;
+  bp.w_ss = strides_of(p).ws;
   bp.q_seg = q_seg;
   bp.kv_seg = kv_seg;
   bp.q_start = q_start;
@@ -372,7 +403,9 @@ csa_status csa_index_gather(const csa_problem* p, const void* k, const int32_t* 
   const int sms = num_sms();
   if (sms <= 0) return CSA_ERR_CUDA;
   const long long n_rows = (long long)p->B * p->S * p->top_k;
-  if (launch_gather(k, idx, out, n_rows, p->S, p->top_k, p->W, p->D, sms, static_cast<cudaStream_t>(stream)) !=
+  const Strides ks = strides_of(p);
+  if (launch_gather(k, ks.kb, ks.kw, idx, out, n_rows, p->S, p->top_k, p->W, p->D, sms,
+                    static_cast<cudaStream_t>(stream)) !=
       cudaSuccess)
     return CSA_ERR_CUDA;
   return CSA_OK;
@@ -411,6 +444,6 @@ const char* csa_status_string(csa_status s) {
   return "unknown status";
 }
 
-int32_t csa_index_abi_version(void) { return 103; }
+int32_t csa_index_abi_version(void) { return 104; }
 
 }  // extern "C"

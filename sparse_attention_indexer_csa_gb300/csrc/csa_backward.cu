@@ -317,7 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int seg = (segs && row_ok) ? p.q_seg[(size_t)d.b * p.S + s] : 0;
       float wc = 0.f;
       if (row_ok) {
-        const size_t off = ((size_t)d.b * p.S + s) * kBH + h;
+        const size_t off = (size_t)d.b * p.w_sb + (size_t)s * p.w_ss + h;
         wc = (p.w_f32 ? reinterpret_cast<const float*>(p.w)[off]
                       : __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p.w)[off])) *
              p.scale;
@@ -678,7 +678,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           bool vis = t < row_thr(p, d.b, s);
           if (vis && segs) vis = p.q_seg[(size_t)d.b * p.S + s] == kvs;
           if (vis) gm = p.g[((size_t)d.b * p.S + s) * p.W + t];
-          const size_t off = ((size_t)d.b * p.S + s) * kBH + 2 * lane;
+          const size_t off = (size_t)d.b * p.w_sb + (size_t)s * p.w_ss + 2 * lane;
           float w0, w1;
           if (p.w_f32) {
             w0 = reinterpret_cast<const float*>(p.w)[off];

@@ -53,8 +53,9 @@ cudaError_t launch_topk(const float* scores, int32_t* idx, long long rows, int W
 int topk_threads(int W);
 
 // Gather of the selected compressed entries (D in {32, 128}).
-cudaError_t launch_gather(const void* k, const int32_t* idx, void* out, long long n_rows, int S, int K, int W, int D,
-                          int sms, cudaStream_t stream);
+// k_sb, k_sw: element strides of k's batch and entry dimensions.
+cudaError_t launch_gather(const void* k, long long k_sb, long long k_sw, const int32_t* idx, void* out,
+                          long long n_rows, int S, int K, int W, int D, int sms, cudaStream_t stream);
 cudaError_t take_status_gather(uint32_t* out, cudaStream_t stream);
 
 // Backward of the score step (csa_backward.cu): the dq / dw kernel over
@@ -70,6 +71,7 @@ struct BwdParams {
   int w_f32;
   float scale;
   const void* w;
+  long long w_sb, w_ss;   // element strides of w's batch and row dimensions
   const int32_t* q_seg;
   const int32_t* kv_seg;
   const int64_t* q_start;

@@ -47,6 +47,7 @@ struct KParams {
   float scale;
   int w_f32;
   const void* w;
+  long long w_sb, w_ss;  // element strides of w's batch and row dimensions
   const int32_t* q_seg;
   const int32_t* kv_seg;
   const int64_t* q_start;
@@ -307,7 +308,7 @@ __device__ void run_scheduler(const KParams& p, const Smem<C>& sm, const WaitCtl
       const int s = s0 + j;
       float v = 0.f;
       if (s < p.S) {
-        const size_t off = ((size_t)b * p.S + s) * H + h;
+        const size_t off = (size_t)b * p.w_sb + (size_t)s * p.w_ss + h;
         v = p.w_f32 ? reinterpret_cast<const float*>(p.w)[off]
                     : __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p.w)[off]);
       }

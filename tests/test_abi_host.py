@@ -39,7 +39,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_abi_version_and_strings(lib):
-    assert lib.csa_index_abi_version() == 103
+    assert lib.csa_index_abi_version() == 104
     for s in range(6):
         assert abi.status_string(s)
     assert abi.status_string(99) == "unknown status"
@@ -65,6 +65,25 @@ def _score(lib, p, q=FAKE, k=FAKE, w=FAKE, qs=None, kvs=None, st=None, out=FAKE)
                                  dict(w_dtype=7), dict(q_layout=2), dict(q_layout=-1)])
 def test_bad_problem_rejected(lib, bad):
     assert _score(lib, _p(**bad)) == abi.CSA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("bad", [dict(q_stride_s=100), dict(q_stride_h=-8), dict(q_stride_b=4), dict(k_stride_w=130),
+                                 dict(k_stride_b=-128), dict(w_stride_s=-1), dict(w_stride_b=-64),
+                                 dict(q_stride_s=1 << 40)])
+def test_bad_strides_rejected(lib, bad):
+    # q and k strides feed TMA maps (multiples of 8 bf16 = 16 bytes); none may be negative
+    assert _score(lib, _p(**bad)) == abi.CSA_ERR_INVALID_ARG
+
+
+def test_good_strides_accepted_by_the_checks(lib):
+    # valid strides pass the argument checks and reach the device query, which
+    # fails only for lack of a device (not an argument error); never run where
+    # a device exists, since the pointers here are fake
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("uses fake pointers; only meaningful without a device")
+    ok = _p(q_stride_s=192 * 128, q_stride_h=128, q_stride_b=192 * 128 * 16, k_stride_w=136, w_stride_s=72)
+    assert _score(lib, ok) != abi.CSA_ERR_INVALID_ARG
 
 
 def test_null_and_misaligned_pointers_rejected(lib):

@@ -89,3 +89,49 @@ def test_gather_reports_out_of_range_indices():
     o = out[0, 0]
     assert torch.equal(o[0], k[0, 0]) and torch.equal(o[1], k[0, 9]) and torch.equal(o[4], k[0, 3])
     assert bool((o[2] == 0).all()) and bool((o[3] == 0).all())
+
+
+def test_strided_views_equal_contiguous_inputs():
+    """q sliced out of a wider [B,S,H',D] projection output, k rows with a
+    padded pitch, w with padded rows: the same scores, selection, gather and
+    backward as contiguous copies of the same values, with no copy made."""
+    wl = WORKLOADS["prefill_4k"].with_(B=2, S=700, W=300, top_k=60, seed=31)
+    inp = make_inputs(wl)
+    B, H, S, D, W = wl.B, wl.H, wl.S, wl.D, wl.W
+    g = torch.Generator().manual_seed(32)
+    big_q = torch.randn(B, S, H + 32, D, generator=g).to(torch.bfloat16)
+    big_q[:, :, 16:16 + H] = inp.q.permute(0, 2, 1, 3)
+    q_view = big_q.cuda()[:, :, 16:16 + H]                      # [B,S,H,D], row pitch (H+32)*D
+    big_k = torch.zeros(B, W + 3, D + 64, dtype=torch.bfloat16)
+    big_k[:, 3:, :D] = inp.k
+    k_view = big_k.cuda()[:, 3:, :D]                             # row pitch D+64, offset 3 rows
+    big_w = torch.zeros(B, S, H + 8, dtype=inp.w.dtype)
+    big_w[:, :, 4:4 + H] = inp.w
+    w_view = big_w.cuda()[:, :, 4:4 + H]                         # row pitch H+8
+    assert not q_view.is_contiguous() and not k_view.is_contiguous() and not w_view.is_contiguous()
+    d = to_dev(inp)
+    q_sm = d["q"].permute(0, 2, 1, 3).contiguous()
+    sm = csa.CSA_Q_SEQ_MAJOR
+    args = (wl.scale, wl.compress_rate)
+    s_ref = csa.index_score(q_sm, d["k"], d["w"], *args, q_layout=sm)
+    s_view = csa.index_score(q_view, k_view, w_view, *args, q_layout=sm)
+    i_ref = csa.index_fused(q_sm, d["k"], d["w"], *args, wl.top_k, q_layout=sm)
+    i_view = csa.index_fused(q_view, k_view, w_view, *args, wl.top_k, q_layout=sm)
+    g_ref = csa.index_gather(d["k"], i_ref)
+    g_view = csa.index_gather(k_view, i_view)
+    cot = torch.randn(B, S, W, generator=torch.Generator().manual_seed(33)).cuda()
+    dq_r, dk_r, dw_r = csa.index_backward(q_sm, d["k"], d["w"], *args, cot, q_layout=sm)
+    dq_v, dk_v, dw_v = csa.index_backward(q_view, k_view, w_view, *args, cot, q_layout=sm)
+    assert_status_ok()
+    assert torch.equal(s_ref, s_view)
+    assert torch.equal(i_ref, i_view)
+    assert torch.equal(g_ref, g_view)
+    assert torch.equal(dq_r, dq_v) and torch.equal(dw_r, dw_v)
+    # dk sums its items' partial products with atomics: equal up to the order of fp32 additions
+    assert torch.allclose(dk_r, dk_v, rtol=0, atol=1e-5 * float(dk_r.abs().max()))
+    check_scores(s_view.cpu().numpy(), oracle_scores(inp))
+    # head-major view: q sliced along heads of a [B,H',S,D] buffer
+    big_h = torch.zeros(B, H + 8, S, D, dtype=torch.bfloat16)
+    big_h[:, 8:] = inp.q
+    q_hv = big_h.cuda()[:, 8:]
+    assert torch.equal(csa.index_fused(q_hv, k_view, w_view, *args, wl.top_k), i_ref)

@@ -78,3 +78,21 @@ def test_replica_inputs_differ_by_rank():
     a = make_inputs(wl.with_(seed=wl.seed + 0))
     b = make_inputs(wl.with_(seed=wl.seed + 1))
     assert not torch.equal(a.q, b.q)
+
+
+def test_row_shard_cut_points():
+    """Row ranges cover every row once, inner cuts on 4-row blocks, and the
+    visible-entry work of the shards is balanced (later rows see more)."""
+    from sparse_attention_indexer_csa_gb300.shard import row_shards, visible_entries
+
+    for S, W, r, n, start in [(16384, 4096, 4, 2, 0), (16384, 4096, 4, 8, 0), (4096, 1024, 4, 3, 0),
+                              (600, 1024, 4, 2, 2000), (10, 4, 4, 4, 0), (7, 100, 1, 2, 0)]:
+        cuts = row_shards(S, W, r, n, start)
+        assert len(cuts) == n and cuts[0][0] == 0 and cuts[-1][1] == S
+        assert all(cuts[i][1] == cuts[i + 1][0] for i in range(n - 1))
+        assert all(b <= e for b, e in cuts)
+        assert all(e % 4 == 0 for _, e in cuts[:-1])
+        work = [sum(visible_entries(s, W, r, start) for s in range(b, e)) for b, e in cuts]
+        if S >= 1024:
+            # a 4-row block of the heaviest rows is the granularity of the balance
+            assert max(work) - min(work) <= 2 * 4 * W, (S, n, work)
