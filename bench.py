@@ -460,7 +460,7 @@ def run_ours(args, wl, inp):
     achieved = wk["flops_nontrivial"] / (avg_launch_ms * 1e-3) / 1e12
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     bound, unit = "tensor", "TFLOP/s"
-    traffic = measured_traffic(wl.name) if args.batch is None else None
+    traffic = measured_traffic(wl.name) if (args.batch is None and args.seed is None) else None
     if wl.name.startswith("decode"):
         # k streaming bound: algorithmic bytes = k + q + w + scores write/read + idx
         bytes_alg = decode_bytes(wl)
@@ -694,6 +694,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--batch", type=int, default=None, help="override B (smaller profiling case)")
+    ap.add_argument("--seed", type=int, default=None, help="override the workload's input seed")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end measurement")
     ap.add_argument("--backward", action="store_true",
                     help="time the backward of the score step instead (its own JSON line)")
@@ -712,6 +713,8 @@ def main():
     wl = WORKLOADS[args.workload]
     if args.batch is not None:
         wl = wl.with_(B=args.batch)
+    if args.seed is not None:
+        wl = wl.with_(seed=args.seed)
     rank = int(os.environ.get("RANK", "0"))
     if args.impl == "reference":
         if rank != 0:

@@ -129,7 +129,9 @@ csa_status csa_index_topk(const csa_problem* p, const float* scores, int32_t* id
  *    rows of its two most recent items of four rows in its slice of the
  *    workspace (2 x 4 x W fp32 per CTA, at most 256 CTAs: a few tens of MB
  *    that stay in L2), so the selection of one item overlaps the scores of
- *    the next; the [B,S,W] score tensor is never formed.
+ *    the next; the [B,S,W] score tensor is never formed.  With segment
+ *    ids a short pre-pass kernel first summarises each item's segment ids
+ *    (64 bytes per item of four rows, after the ring in the workspace).
  *  - otherwise (decode-style single rows, long rows): the scores go to the
  *    workspace ([B,S,W] fp32) and a second kernel selects.
  * scores_dbg [B,S,W] fp32, if non-NULL, also receives the exact fp32 scores

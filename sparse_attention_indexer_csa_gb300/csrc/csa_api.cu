@@ -94,6 +94,12 @@ size_t fused_ring_bytes(const csa_problem* p) {
   const long long ctas = std::min<long long>(items, kMaxGrid);
   return (size_t)ctas * 2 * 4 * (size_t)w_pad_of(p) * sizeof(float);
 }
+// Segment summaries of the one-kernel fused path (one per item of four rows),
+// after the ring in the same workspace.
+size_t fused_seginfo_bytes(const csa_problem* p) {
+  return (size_t)p->B * (size_t)((p->S + 3) / 4) * sizeof(SegInfo);
+}
+size_t fused_seginfo_offset(const csa_problem* p) { return (fused_ring_bytes(p) + 255) & ~(size_t)255; }
 
 int num_sms() {
   static int cached[64];
@@ -175,7 +181,7 @@ int bwd_chunk_pairs(const csa_problem* p, int sms) {
 
 csa_status run_index_kernel(const csa_problem* p, bool fused, const void* q, const void* k, const void* w,
                             const int32_t* q_seg, const int32_t* kv_seg, const int64_t* q_start, float* scores,
-                            int32_t* idx, float* ring, cudaStream_t stream) {
+                            int32_t* idx, float* ring, cudaStream_t stream, SegInfo* seginfo = nullptr) {
   const bool row_kernel = use_row_kernel(p);
   KernelChoice kc{p->H, p->D, row_kernel ? 1 : 4, fused};
   CUtensorMap tq, tk;
@@ -212,13 +218,18 @@ csa_status run_index_kernel(const csa_problem* p, bool fused, const void* q, con
   const int sms = num_sms();
   if (sms <= 0) return CSA_ERR_CUDA;
   const int grid = (int)std::min<long long>(items, std::min(sms, kMaxGrid));
+  if (seginfo != nullptr && q_seg != nullptr && kc.R == 4 && kp.n_chunks == 1) {
+    // segment ids scanned once per item across the whole GPU, ahead of the kernel
+    if (launch_segscan(kp, seginfo, sms, stream) != cudaSuccess) return CSA_ERR_CUDA;
+    kp.seginfo = seginfo;
+  }
   if (launch_index_kernel(kc, tq, tk, kp, grid, stream) != cudaSuccess) return CSA_ERR_CUDA;
   return CSA_OK;
 }
 
 size_t fused_workspace_bytes(const csa_problem* p) {
   if (check_problem(p) != CSA_OK) return 0;
-  if (fused_one_kernel(p)) return fused_ring_bytes(p);
+  if (fused_one_kernel(p)) return fused_seginfo_offset(p) + fused_seginfo_bytes(p);
   return (size_t)p->B * p->S * p->W * sizeof(float);
 }
 
@@ -299,8 +310,10 @@ csa_status csa_index_fused(const csa_problem* p, const void* q, const void* k, c
   const size_t need = fused_workspace_bytes(p);
   if (fused_one_kernel(p)) {
     if (workspace == nullptr || workspace_bytes < need || !aligned(workspace, 16)) return CSA_ERR_INVALID_ARG;
+    SegInfo* seginfo =
+        reinterpret_cast<SegInfo*>(static_cast<uint8_t*>(workspace) + fused_seginfo_offset(p));
     return run_index_kernel(p, true, q, k, w, q_seg, kv_seg, q_start, scores_dbg, idx,
-                            static_cast<float*>(workspace), s);
+                            static_cast<float*>(workspace), s, seginfo);
   }
   // Long rows or single-row problems: scores through the workspace (or the
   // caller's debug copy), then the selection kernel.

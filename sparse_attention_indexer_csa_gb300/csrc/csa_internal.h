@@ -46,6 +46,8 @@ cudaError_t launch_index_kernel(const KernelChoice& kc, const CUtensorMap& tq, c
                                 const KParams& p, int grid, cudaStream_t stream);
 // Dynamic shared memory of that kernel (0 if the choice is not instantiated).
 size_t index_kernel_smem(const KernelChoice& kc, int w_pad);
+// Segment pre-pass of the fused path: SegInfo of every item of four rows.
+cudaError_t launch_segscan(const KParams& p, SegInfo* out, int sms, cudaStream_t stream);
 
 // Standalone per-row selection over [rows, W] fp32 scores.
 cudaError_t launch_topk(const float* scores, int32_t* idx, long long rows, int W, int K,

@@ -7,6 +7,36 @@ namespace csa {
 
 namespace {
 
+// Segment pre-pass of the one-kernel fused path: one warp per item of four
+// whole rows scans the item's segment ids and writes its SegInfo, so the
+// persistent kernel's scheduler warps read a summary instead of scanning
+// up to W ids per item themselves.
+__global__ void __launch_bounds__(256) csa_segscan_kernel(const KParams p, SegInfo* out) {
+  const int warp = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+  const int n_warps = (int)((gridDim.x * blockDim.x) >> 5);
+  const long long n = (long long)p.B * p.n_rb;
+  for (long long i = warp; i < n; i += n_warps) {
+    const int b = (int)(i / p.n_rb), rb = (int)(i % p.n_rb);
+    int thr[4], seg[4], nvis[4], tfirst[4], contig[4];
+    const int thr_max = item_rows<4>(p, b, rb * 4, thr, seg);
+    int t_lo, t_hi;
+    scan_segments<4>(p, b, 0, min(p.n_tiles * kTileT, thr_max), thr, seg, nvis, tfirst, contig, t_lo, t_hi);
+    if (lane_id() == 0) {
+      SegInfo si;
+      si.t_lo = t_lo;
+      si.t_hi = t_hi;
+      si.pad0 = si.pad1 = 0;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        si.nvis[j] = nvis[j];
+        si.tfirst[j] = tfirst[j];
+        si.contig[j] = contig[j];
+      }
+      out[i] = si;
+    }
+  }
+}
+
 template <class C>
 cudaError_t launch_cfg(const CUtensorMap& tq, const CUtensorMap& tk, const KParams& p, int grid,
                        cudaStream_t stream) {
@@ -47,6 +77,14 @@ size_t index_kernel_smem(const KernelChoice& kc, int w_pad) {
   CSA_DISPATCH(4, 32, 4, false, return smem_cfg<C>(w_pad))
   CSA_DISPATCH(4, 32, 4, true, return smem_cfg<C>(w_pad))
   return 0;
+}
+
+cudaError_t launch_segscan(const KParams& p, SegInfo* out, int sms, cudaStream_t stream) {
+  const long long items = (long long)p.B * p.n_rb;
+  const long long blocks = (items + 7) / 8;  // eight warps per block, one item each
+  const int grid = (int)std::min<long long>(std::max<long long>(blocks, 1), (long long)sms * 16);
+  csa_segscan_kernel<<<grid, 256, 0, stream>>>(p, out);
+  return cudaGetLastError();
 }
 
 cudaError_t take_status_prefill(uint32_t* out, cudaStream_t stream) {

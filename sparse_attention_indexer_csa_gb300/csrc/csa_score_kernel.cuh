@@ -42,6 +42,14 @@ namespace csa {
 
 constexpr int kTileT = 128;  // compressed entries per tile (UMMA M)
 
+// Per-item segment summary written by csa_segscan_kernel for whole-row items
+// of four rows (64 bytes): tiles holding visible entries, and per row the
+// visible count, first visible entry and contiguity.
+struct SegInfo {
+  int t_lo, t_hi, pad0, pad1;
+  int nvis[4], tfirst[4], contig[4];
+};
+
 struct KParams {
   int B, S, W, r, K;
   float scale;
@@ -54,6 +62,7 @@ struct KParams {
   float* scores;  // score mode: output; fused: optional debug copy
   int32_t* idx;   // fused: selection output
   float* ring;    // fused: per-CTA staging of two items' score rows [grid][2][R][w_pad]
+  const SegInfo* seginfo;  // with segment ids and whole-row items: [B][n_rb] summaries, or null
   int n_rb, n_tiles, n_chunks, chunk_tiles, n_items;
   int w_pad;  // fused: row pitch (floats) of the shared score rows
   unsigned long long wait_ns;
@@ -179,6 +188,103 @@ __device__ __forceinline__ void item_coords(const KParams& p, int item, int& b, 
 }
 
 // Scheduler warp `sw` (0 or 1) prepares the items with it % 2 == sw.
+// Rows s0 .. s0+R-1 of batch b: each row's visible bound min(W, (pos+1)/r)
+// under the future mask (0 for rows past S) and its segment id (0 without
+// segments); returns the largest bound.
+template <int R>
+__device__ __forceinline__ int item_rows(const KParams& p, int b, int s0, int (&thr)[R], int (&seg)[R]) {
+  const long long qs0 = p.q_start ? (long long)p.q_start[b] : 0ll;
+  int thr_max = 0;
+#pragma unroll
+  for (int j = 0; j < R; ++j) {
+    const int s = s0 + j;
+    long long tv = 0;
+    if (s < p.S) {
+      tv = (qs0 + s + 1) / p.r;
+      tv = tv < 0 ? 0 : (tv > p.W ? p.W : tv);
+    }
+    thr[j] = (int)tv;
+    seg[j] = (p.q_seg != nullptr && s < p.S) ? p.q_seg[(size_t)b * p.S + s] : 0;
+    thr_max = max(thr_max, thr[j]);
+  }
+  return thr_max;
+}
+
+// Segment scan of one item (a warp): over entries [e_lo, e_hi) of batch b,
+// per row j the entries visible under both masks -- count, first entry and
+// whether they form one contiguous run -- and the tiles [t_lo, t_hi) that
+// hold any of them (t_lo = t_hi when none does).  Segment ids are read with
+// 16-byte loads, four in flight per lane, when they are aligned.
+template <int R>
+__device__ void scan_segments(const KParams& p, int b, int e_lo, int e_hi, const int (&thr)[R], const int (&seg)[R],
+                              int (&nvis)[R], int (&tfirst)[R], int (&contig)[R], int& t_lo, int& t_hi) {
+  const uint32_t lane = lane_id();
+  t_lo = t_hi = e_lo / kTileT;
+  int cnt[R], tmn[R], tmx[R];
+#pragma unroll
+  for (int j = 0; j < R; ++j) {
+    cnt[j] = 0;
+    tmn[j] = 0x7FFFFFFF;
+    tmx[j] = -1;
+  }
+  const int32_t* kv = p.kv_seg + (size_t)b * p.W;
+  const bool vec = ((reinterpret_cast<uintptr_t>(kv) & 15u) == 0) && (e_lo % 4 == 0);
+  auto visit = [&](int t, int ks) {
+#pragma unroll
+    for (int j = 0; j < R; ++j) {
+      const bool m = (t < thr[j]) && (ks == seg[j]);
+      cnt[j] += m;
+      if (m) {
+        tmn[j] = min(tmn[j], t);
+        tmx[j] = max(tmx[j], t);
+      }
+    }
+  };
+  if (vec) {
+    // four 16-byte loads in flight per lane per round (512 entries per warp)
+    for (int t0 = e_lo + 4 * (int)lane; t0 < e_hi; t0 += 512) {
+      int4 v4[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int t = t0 + 128 * u;
+        v4[u] = (t + 3 < e_hi) ? *reinterpret_cast<const int4*>(kv + t) : make_int4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int t = t0 + 128 * u;
+        if (t + 3 < e_hi) {
+          visit(t, v4[u].x);
+          visit(t + 1, v4[u].y);
+          visit(t + 2, v4[u].z);
+          visit(t + 3, v4[u].w);
+        } else {
+          for (int x = t; x < e_hi; ++x) visit(x, kv[x]);
+        }
+      }
+    }
+  } else {
+    for (int t = e_lo + (int)lane; t < e_hi; t += 32) visit(t, kv[t]);
+  }
+  int tmin = 0x7FFFFFFF, tmax = -1;
+#pragma unroll
+  for (int j = 0; j < R; ++j) {
+    nvis[j] = (int)__reduce_add_sync(0xFFFFFFFFu, (unsigned)cnt[j]);
+    tfirst[j] = __reduce_min_sync(0xFFFFFFFFu, tmn[j]);
+    const int last = __reduce_max_sync(0xFFFFFFFFu, tmx[j]);
+    contig[j] = (nvis[j] == 0) || (last - tfirst[j] + 1 == nvis[j]);
+    if (nvis[j] > 0) {
+      tmin = min(tmin, tfirst[j]);
+      tmax = max(tmax, last);
+    } else {
+      tfirst[j] = 0;
+    }
+  }
+  if (tmax >= 0) {
+    t_lo = tmin / kTileT;
+    t_hi = tmax / kTileT + 1;
+  }
+}
+
 template <class C>
 __device__ void run_scheduler(const KParams& p, const Smem<C>& sm, const WaitCtl& ctl, int sw) {
   constexpr int R = C::R, H = C::H;
@@ -201,21 +307,8 @@ __device__ void run_scheduler(const KParams& p, const Smem<C>& sm, const WaitCtl
       item_coords(p, item, b, rb, c);
     }
     const int s0 = rb * R;
-    const long long qs0 = p.q_start ? (long long)p.q_start[b] : 0ll;
     int thr[R], seg[R], nvis[R], tfirst[R], contig[R];
-    int thr_max = 0;
-#pragma unroll
-    for (int j = 0; j < R; ++j) {
-      const int s = s0 + j;
-      long long tv = 0;
-      if (s < p.S) {
-        tv = (qs0 + s + 1) / p.r;
-        tv = tv < 0 ? 0 : (tv > p.W ? p.W : tv);
-      }
-      thr[j] = (int)tv;
-      seg[j] = (segs && s < p.S) ? p.q_seg[(size_t)b * p.S + s] : 0;
-      thr_max = max(thr_max, thr[j]);
-    }
+    const int thr_max = item_rows<R>(p, b, s0, thr, seg);
     const int c_lo = c * p.chunk_tiles;
     const int c_hi = min(p.n_tiles, c_lo + p.chunk_tiles);
     int t_lo = c_lo, t_hi = c_lo;
@@ -227,72 +320,18 @@ __device__ void run_scheduler(const KParams& p, const Smem<C>& sm, const WaitCtl
         contig[j] = 1;
       }
       t_hi = max(c_lo, min(c_hi, (thr_max + kTileT - 1) / kTileT));
+    } else if (p.seginfo != nullptr) {  // scanned ahead by csa_segscan_kernel (whole-row items)
+      const SegInfo& si = p.seginfo[(size_t)b * p.n_rb + rb];
+#pragma unroll
+      for (int j = 0; j < R; ++j) {
+        nvis[j] = si.nvis[j];
+        tfirst[j] = si.tfirst[j];
+        contig[j] = si.contig[j];
+      }
+      t_lo = si.t_lo;
+      t_hi = si.t_hi;
     } else {
-      int cnt[R], tmn[R], tmx[R];
-#pragma unroll
-      for (int j = 0; j < R; ++j) {
-        cnt[j] = 0;
-        tmn[j] = 0x7FFFFFFF;
-        tmx[j] = -1;
-      }
-      const int e_lo = c_lo * kTileT;
-      const int e_hi = min(c_hi * kTileT, thr_max);
-      const int32_t* kv = p.kv_seg + (size_t)b * p.W;
-      const bool vec = ((reinterpret_cast<uintptr_t>(kv) & 15u) == 0) && (e_lo % 4 == 0);
-      auto visit = [&](int t, int ks) {
-#pragma unroll
-        for (int j = 0; j < R; ++j) {
-          const bool m = (t < thr[j]) && (ks == seg[j]);
-          cnt[j] += m;
-          if (m) {
-            tmn[j] = min(tmn[j], t);
-            tmx[j] = max(tmx[j], t);
-          }
-        }
-      };
-      if (vec) {
-        // four 16-byte loads in flight per lane per round (512 entries per warp)
-        for (int t0 = e_lo + 4 * (int)lane; t0 < e_hi; t0 += 512) {
-          int4 v4[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int t = t0 + 128 * u;
-            v4[u] = (t + 3 < e_hi) ? *reinterpret_cast<const int4*>(kv + t) : make_int4(0, 0, 0, 0);
-          }
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int t = t0 + 128 * u;
-            if (t + 3 < e_hi) {
-              visit(t, v4[u].x);
-              visit(t + 1, v4[u].y);
-              visit(t + 2, v4[u].z);
-              visit(t + 3, v4[u].w);
-            } else {
-              for (int x = t; x < e_hi; ++x) visit(x, kv[x]);
-            }
-          }
-        }
-      } else {
-        for (int t = e_lo + (int)lane; t < e_hi; t += 32) visit(t, kv[t]);
-      }
-      int tmin = 0x7FFFFFFF, tmax = -1;
-#pragma unroll
-      for (int j = 0; j < R; ++j) {
-        nvis[j] = (int)__reduce_add_sync(0xFFFFFFFFu, (unsigned)cnt[j]);
-        tfirst[j] = __reduce_min_sync(0xFFFFFFFFu, tmn[j]);
-        const int last = __reduce_max_sync(0xFFFFFFFFu, tmx[j]);
-        contig[j] = (nvis[j] == 0) || (last - tfirst[j] + 1 == nvis[j]);
-        if (nvis[j] > 0) {
-          tmin = min(tmin, tfirst[j]);
-          tmax = max(tmax, last);
-        } else {
-          tfirst[j] = 0;
-        }
-      }
-      if (tmax >= 0) {
-        t_lo = tmin / kTileT;
-        t_hi = tmax / kTileT + 1;
-      }
+      scan_segments<R>(p, b, c_lo * kTileT, min(c_hi * kTileT, thr_max), thr, seg, nvis, tfirst, contig, t_lo, t_hi);
     }
     int trivial = 0;
     if (C::FUSED && p.scores == nullptr) {
@@ -301,9 +340,10 @@ __device__ void run_scheduler(const KParams& p, const Smem<C>& sm, const WaitCtl
       for (int j = 0; j < R; ++j) trivial &= (nvis[j] <= p.K) ? 1 : 0;
       if (trivial) t_hi = t_lo;
     }
-    // stage the weights (fp32) of the item's rows; rows past S get 0
+    // stage the weights (fp32) of the item's rows; rows past S get 0 (an item
+    // whose rows keep every visible entry computes no score and needs none)
     float* ws = sm.w(slot);
-    for (int i = (int)lane; i < R * H; i += 32) {
+    for (int i = (int)lane; i < (trivial ? 0 : R * H); i += 32) {
       const int j = i / H, h = i % H;
       const int s = s0 + j;
       float v = 0.f;

@@ -113,9 +113,11 @@ def test_fused_large_w_needs_workspace(lib):
     assert need == 64 * 1 * 32768 * 4
     assert lib.csa_index_fused(ctypes.byref(p), FAKE, FAKE, FAKE, None, None, None, FAKE, None, None, 0,
                                None) == abi.CSA_ERR_INVALID_ARG
-    # one-kernel path: a two-item staging ring per CTA (at most 256 CTAs)
-    assert abi.workspace_size(_p(W=4096, S=16384), 1) == 256 * 2 * 4 * 4096 * 4
-    assert abi.workspace_size(_p(W=100, S=8), 1) == 2 * 2 * 4 * 128 * 4
+    # one-kernel path: a two-item staging ring per CTA (at most 256 CTAs),
+    # then (256-byte aligned) a 64-byte segment summary per item of four rows
+    assert abi.workspace_size(_p(W=4096, S=16384), 1) == 256 * 2 * 4 * 4096 * 4 + 1 * 4096 * 64
+    ring = 2 * 2 * 4 * 128 * 4
+    assert abi.workspace_size(_p(W=100, S=8), 1) == (ring + 255) // 256 * 256 + 2 * 64
     assert abi.workspace_size(_p(), 0) == 0
     assert abi.workspace_size(_p(B=0), 1) == 0
 
