@@ -476,9 +476,12 @@ __device__ void run_mma(const KParams& p, const Smem<C>& sm, const WaitCtl& ctl,
 }
 
 // Accumulate this warp's rows over heads from one TMEM accumulator buffer.
-template <class C>
+// `loaded()` runs once every TMEM load of the buffer has completed, before
+// the arithmetic on the last chunk, so the buffer can go back to the MMA
+// issuer early.
+template <class C, class F>
 __device__ __forceinline__ void epilogue_accumulate(uint32_t t_row, const float* ws, int hf,
-                                                    float (&acc)[C::RW]) {
+                                                    float (&acc)[C::RW], F&& loaded) {
   constexpr int H = C::H, RW = C::RW;
 #pragma unroll
   for (int jj = 0; jj < RW; ++jj) acc[jj] = 0.f;
@@ -512,6 +515,7 @@ __device__ __forceinline__ void epilogue_accumulate(uint32_t t_row, const float*
       if (hh == 1)
         acc[jj] = ((a[0].x + a[0].y) + (a[1].x + a[1].y)) + ((a[2].x + a[2].y) + (a[3].x + a[3].y));
       if (c + 1 < 2 * RW) tmem_wait32(nxt);
+      if (c + 2 == 2 * RW) loaded();  // the last chunk is in registers
     }
   } else {
     static_assert((C::RW * H) % 8 == 0, "small-head path loads 8 columns at a time");
@@ -526,6 +530,7 @@ __device__ __forceinline__ void epilogue_accumulate(uint32_t t_row, const float*
         acc[jj] = fmaf(ws[(hf * RW + jj) * H + h], fmaxf(v[i], 0.f), acc[jj]);
       }
     }
+    loaded();
   }
 }
 
@@ -607,10 +612,15 @@ __device__ void run_epilogue(const KParams& p, const Smem<C>& sm, const WaitCtl&
         const int a = acount & 1;
         const bool ok = mbar_wait(sm.acc_full(a), (acount >> 1) & 1, ctl);
         tc_fence_after();
-        if (ok) epilogue_accumulate<C>(t_lane + (uint32_t)(a * C::N), ws, hf, acc);
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(sm.acc_empty(a));
+        bool released = false;
+        auto release = [&]() {  // every TMEM read of accumulator a has completed
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(sm.acc_empty(a));
+          released = true;
+        };
+        if (ok) epilogue_accumulate<C>(t_lane + (uint32_t)(a * C::N), ws, hf, acc, release);
+        if (!released) release();
         ++acount;
       }
       int kvs = 0;
