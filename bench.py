@@ -317,13 +317,25 @@ def run_ours(args, wl, inp):
     idx = torch.empty(wl.B, S_local, wl.top_k, dtype=torch.int32, device=dev)
     ws_bytes = csa.workspace_size(p, 1)
     ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev) if ws_bytes else None
-    # decode-style single rows and rows longer than 4096 take two kernels
-    launches_per_step = 2 if (wl.S <= 2 or wl.W > 4096) else 1
+    # decode-style single rows and rows longer than 16384 take two kernels;
+    # segment ids add the summary pre-pass
+    launches_per_step = (2 if (wl.S <= 2 or wl.W > 16384 or args.two_pass) else 1) + \
+        (1 if (inp.q_seg is not None and wl.S > 2 and wl.W <= 16384 and not args.two_pass) else 0)
+
+    two_pass = args.two_pass
+    if two_pass:  # the scores through HBM, then the selection kernel: for comparison only
+        sc_buf = torch.empty(wl.B, S_local, wl.W, dtype=torch.float32, device=dev)
+        pt = csa.Problem(wl.B, 1, S_local, 1, wl.W, 1, 1.0, wl.top_k, csa.CSA_F32, csa.CSA_Q_HEAD_MAJOR)
 
     def step():
         if S_local == 0:  # an empty row shard
             return
-        st = csa.index_fused_raw(p, q, k, w, q_seg, kv_seg, q_start, idx, None, ws, stream)
+        if two_pass:
+            st = csa.index_score_raw(p, q, k, w, q_seg, kv_seg, q_start, sc_buf, stream)
+            if st == csa.CSA_OK:
+                st = csa.index_topk_raw(pt, sc_buf, idx, None, stream)
+        else:
+            st = csa.index_fused_raw(p, q, k, w, q_seg, kv_seg, q_start, idx, None, ws, stream)
         if st != csa.CSA_OK:
             raise RuntimeError(f"csa_index_fused returned {st}")
 
@@ -493,6 +505,8 @@ def run_ours(args, wl, inp):
     }
     if shard_check is not None:
         line["shard_check"] = shard_check
+    if args.two_pass:
+        line["mode"] = "two-pass comparison: scores [B,S,W] fp32 through HBM, then the selection kernel"
     if args.gather:  # gather of the selected rows, timed on its own over the same selection
         gout = torch.empty(wl.B, wl.S, wl.top_k, wl.D, dtype=torch.bfloat16, device=dev)
         for _ in range(3):
@@ -703,6 +717,9 @@ def main():
     ap.add_argument("--shard", default="replicas", choices=["replicas", "rows"],
                     help="under torchrun: independent replicas per rank (weak scaling) or one problem whose "
                          "query rows are split over the ranks (strong scaling)")
+    ap.add_argument("--two-pass", action="store_true",
+                    help="time the score kernel then the selection kernel over stored scores instead of the "
+                         "fused path (comparison only)")
     ap.add_argument("--no-side", action="store_true",
                     help="skip the decode and packed-document legs reported beside the headline")
     ap.add_argument("--gather", action="store_true",

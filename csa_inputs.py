@@ -60,7 +60,8 @@ def _cfg(name, B, S, r, H, D, top_k, w_dtype, sigma_w, W=None, q_start=None, doc
 
 
 # The five workloads: a tiny parity case, a mid-size prefill, the long-context
-# prefill (sequence 16384), packed documents and single-row decode.
+# prefill (sequence 16384), packed documents and single-row decode; then two
+# longer prefills (sequences 32768 and 65536).
 WORKLOADS = {
     "tiny": _cfg("tiny", 1, 256, 4, 4, 32, 16, "f32", 0.5),
     "prefill_4k": _cfg("prefill_4k", 1, 4096, 4, 64, 128, 512, "bf16", 1.0 / 8),
@@ -68,6 +69,10 @@ WORKLOADS = {
     "packed_8k": _cfg("packed_8k", 4, 8192, 4, 64, 128, 1024, "bf16", 1.0 / 8, docs=(3, 8)),
     "decode_32k": _cfg("decode_32k", 64, 1, 4, 64, 128, 2048, "bf16", 1.0 / 8,
                        W=32768, q_start=131071),
+    # longer prefills (rows of up to 8192 / 16384 compressed entries), the
+    # same distributions: the fused kernel's long-row mode
+    "prefill_32k": _cfg("prefill_32k", 1, 32768, 4, 64, 128, 2048, "bf16", 1.0 / 8),
+    "prefill_64k": _cfg("prefill_64k", 1, 65536, 4, 64, 128, 2048, "bf16", 1.0 / 8),
 }
 
 

@@ -16,6 +16,7 @@ namespace csa {
 namespace {
 
 constexpr int kFusedMaxW = 4096;   // shared-memory score rows of the fused kernel
+constexpr int kFusedLongMaxW = 16384;  // its long-row mode: one shared row, selected by a team
 constexpr int kMaxGrid = 256;      // CTAs of the persistent kernel (bounds the fused staging ring)
 constexpr int kTopkMaxW = 49152;   // one row staged in shared memory by the top-k kernel
 constexpr int kDecodeChunkTiles = 8;
@@ -84,7 +85,13 @@ bool use_row_kernel(const csa_problem* p) { return p->S <= 2 && p->H == 64 && p-
 
 // Fused in one kernel (selection on the SM) unless the problem is single-row
 // or its rows are too long for shared memory; those go through two passes.
-bool fused_one_kernel(const csa_problem* p) { return !use_row_kernel(p) && p->W <= kFusedMaxW; }
+// Rows of 4097..16384 entries take the kernel's long-row mode (H = 64, D = 128).
+bool fused_long(const csa_problem* p) {
+  return !use_row_kernel(p) && p->W > kFusedMaxW && p->W <= kFusedLongMaxW && p->H == 64 && p->D == 128;
+}
+bool fused_one_kernel(const csa_problem* p) {
+  return !use_row_kernel(p) && (p->W <= kFusedMaxW || fused_long(p));
+}
 
 int w_pad_of(const csa_problem* p) { return ((p->W + kTileT - 1) / kTileT) * kTileT; }
 
@@ -184,6 +191,7 @@ csa_status run_index_kernel(const csa_problem* p, bool fused, const void* q, con
                             int32_t* idx, float* ring, cudaStream_t stream, SegInfo* seginfo = nullptr) {
   const bool row_kernel = use_row_kernel(p);
   KernelChoice kc{p->H, p->D, row_kernel ? 1 : 4, fused};
+  kc.long_rows = fused && p->W > kFusedMaxW;
   CUtensorMap tq, tk;
   if (!make_q_map(&tq, p, q, kc.R) || !make_k_map(&tk, p, k)) return CSA_ERR_CUDA;
   KParams kp;

@@ -39,6 +39,7 @@ cudaError_t smem_limit_once(int bytes) {
 struct KernelChoice {
   int H, D, R;
   bool fused;
+  bool long_rows = false;  // fused with rows of 4097..16384 entries
 };
 
 // Launch the persistent score (or fused score + selection) kernel.

@@ -87,16 +87,26 @@ struct FusedRowScratch {
   BinScratch<512, 256, 128> bs;  // rows of up to 4096 entries
 };
 
+// Long-row mode (rows of up to 16384 entries): the select warps select as one
+// team of 128 threads, one row at a time, from a single shared row buffer.
+constexpr int kLongMaxW = 16384;
+struct LongRowScratch {
+  SelectScratch sc[4];                          // per warp (visible-set writes); sc[0] for the team
+  BinScratch<1024, 1024, kLongMaxW / 32> bs;    // the team's binned search
+};
+
 constexpr uint32_t pow2_cols(uint32_t n) {
   uint32_t c = 32;
   while (c < n) c <<= 1;
   return c;
 }
 
-template <int H_, int D_, int R_, bool FUSED_>
+template <int H_, int D_, int R_, bool FUSED_, bool LONG_ = false>
 struct Cfg {
   static constexpr int H = H_, D = D_, R = R_;
   static constexpr bool FUSED = FUSED_;
+  static constexpr bool LONG = LONG_;  // fused, rows of 4097..16384 entries
+  static_assert(!LONG || (FUSED && R_ == 4), "long-row mode is the fused four-row kernel");
   static constexpr int N = R * H;
   static_assert(N % 16 == 0 && N >= 16 && N <= 256, "UMMA N must be 16..256 in steps of 16");
   static constexpr int KC = (D % 64 == 0) ? 64 : 32;  // K elements per swizzled row
@@ -129,12 +139,11 @@ struct Cfg {
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;  // tmem base, abort flag
   static constexpr uint32_t OFF_STATS = (OFF_MISC + 16 + 15) & ~15u;  // RowStats[2][R]
   static constexpr uint32_t OFF_SCR = (OFF_STATS + 2 * R * sizeof(RowStats) + 15) & ~15u;
-  static constexpr uint32_t NSCR = SW;
-  static constexpr uint32_t OFF_SROW = (OFF_SCR + NSCR * sizeof(FusedRowScratch) + 127) & ~127u;
+  static constexpr uint32_t SCR_BYTES = LONG ? (uint32_t)sizeof(LongRowScratch) : SW * (uint32_t)sizeof(FusedRowScratch);
+  static constexpr uint32_t OFF_SROW = (OFF_SCR + SCR_BYTES + 127) & ~127u;
+  static constexpr uint32_t SROWS = FUSED ? (LONG ? 1u : (uint32_t)R) : 0u;  // shared score rows
   // dynamic shared memory for a given fused row pitch (+1 KB alignment slack)
-  static constexpr uint32_t smem_bytes(int w_pad) {
-    return OFF_SROW + (FUSED ? (uint32_t)R * (uint32_t)w_pad * 4u : 0u) + 1024u;
-  }
+  static constexpr uint32_t smem_bytes(int w_pad) { return OFF_SROW + SROWS * (uint32_t)w_pad * 4u + 1024u; }
 };
 
 template <class C>
@@ -172,6 +181,7 @@ struct Smem {
   __device__ FusedRowScratch* scratch(int j) const {
     return reinterpret_cast<FusedRowScratch*>(base + C::OFF_SCR) + j;
   }
+  __device__ LongRowScratch* long_scratch() const { return reinterpret_cast<LongRowScratch*>(base + C::OFF_SCR); }
   __device__ float* srow(int j, int w_pad) const {
     return reinterpret_cast<float*>(base + C::OFF_SROW) + (size_t)j * w_pad;
   }
@@ -729,6 +739,73 @@ __device__ void run_selector(const KParams& p, const Smem<C>& sm, const WaitCtl&
   }
 }
 
+// Long-row mode: the R select warps form one team.  Trivial items: each warp
+// writes its own row's visible set.  Scored items: the team copies the
+// item's staged rows into the single shared row buffer one at a time and
+// selects each; the staging slot goes back to the epilogue once its last
+// row has been copied.
+template <class C>
+__device__ void run_selector_long(const KParams& p, const Smem<C>& sm, const WaitCtl& ctl, int j) {
+  constexpr int R = C::R;
+  constexpr uint32_t kSelBar = 6;  // named barrier of the select team
+  const uint32_t lane = lane_id();
+  const Team<32> wteam{0u, lane};
+  const Team<32 * R> team{kSelBar, (uint32_t)j * 32u + lane};
+  LongRowScratch* ls = sm.long_scratch();
+  float* srow = sm.srow(0, p.w_pad);
+  uint32_t nt = 0, nc = 0;  // scored items, row copies
+  int it = 0;
+  for (int item = blockIdx.x; item < p.n_items; item += gridDim.x, ++it) {
+    const int slot = it % C::SLOTS;
+    mbar_wait(sm.item_full(slot), (it / C::SLOTS) & 1, ctl);
+    const ItemDesc<R>* d = sm.desc(slot);
+    const int b = d->b, s0 = d->s0;
+    if (d->trivial) {
+      const int s = s0 + j;
+      if (s < p.S)
+        write_visible_set<32>(p.idx + ((size_t)b * p.S + s) * p.K, p.K, d->nvis[j], d->tfirst[j], d->contig[j],
+                              d->thr[j], d->seg[j], p.kv_seg + (size_t)b * p.W, &ls->sc[j], wteam);
+    } else {
+      const int rs = (int)(nt & 1u);
+      const int t_lo = d->t_lo, t_hi = d->t_hi;
+      const int e0 = t_lo * kTileT, n = (t_hi - t_lo) * kTileT;
+      const uint32_t row_bytes = (uint32_t)n * 4u;
+      mbar_wait(sm.ring_full(rs), (nt >> 1) & 1u, ctl);
+      RowStats st[R];
+#pragma unroll
+      for (int r = 0; r < R; ++r) st[r] = *sm.stats(rs, r);
+      team.sync();  // every thread holds the statistics
+      if (team.tid == 0) {
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+          RowStats* stp = sm.stats(rs, r);
+          stp->nvis = 0u;
+          stp->min_key = 0xFFFFFFFFu;
+          stp->max_key = 0u;
+        }
+        fence_proxy_async_global();
+      }
+      const float* src = p.ring + ((size_t)blockIdx.x * 2 + rs) * R * p.w_pad;
+      for (int r = 0; r < R; ++r) {
+        if (team.tid == 0) {
+          mbar_arrive_expect_tx(sm.copy_full(), row_bytes);
+          if (row_bytes > 0u) bulk_copy_g2s(srow + e0, src + (size_t)r * p.w_pad + e0, row_bytes, sm.copy_full());
+        }
+        mbar_wait(sm.copy_full(), nc & 1u, ctl);
+        ++nc;
+        if (r == R - 1 && team.tid == 0) mbar_arrive(sm.ring_empty(rs));  // every row of the slot is copied
+        if (s0 + r < p.S)
+          team_topk_row(srow, e0, n, (uint32_t)p.K, st[r], p.idx + ((size_t)b * p.S + s0 + r) * p.K, &ls->bs,
+                        &ls->sc[0], team);
+        team.sync();  // the row buffer may be refilled
+      }
+      ++nt;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(sm.item_empty(slot));
+  }
+}
+
 template <class C>
 __global__ void __launch_bounds__(C::NTHREADS, 1)
     csa_index_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
@@ -794,7 +871,10 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
   } else if (warp < 4 + C::EW) {
     run_epilogue<C>(p, sm, ctl, tmem_base, warp - 4);
   } else {
-    if constexpr (C::FUSED) run_selector<C>(p, sm, ctl, warp - 4 - C::EW);
+    if constexpr (C::LONG)
+      run_selector_long<C>(p, sm, ctl, warp - 4 - C::EW);
+    else if constexpr (C::FUSED)
+      run_selector<C>(p, sm, ctl, warp - 4 - C::EW);
   }
   __syncwarp();
   tc_fence_before();

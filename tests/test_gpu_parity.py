@@ -313,3 +313,66 @@ def test_invalid_arguments_on_device_tensors():
     p.scale = 0.1
     p.H = 8
     assert csa.index_score_raw(p, d["q"], d["k"], d["w"], None, None, None, out) == csa.CSA_ERR_UNSUPPORTED
+
+
+# --------------------------------------------------------------------------- long rows (4096 < W <= 16384)
+LONG = [
+    # rows of about 7500-7750 visible entries (offset positions), W = 8192
+    dict(B=1, S=1024, W=8192, r=4, top_k=2048, q_start=30000),
+    # rows of about 15500-15750 visible entries, W = 16384 (the mode's maximum)
+    dict(B=1, S=1024, W=16384, r=4, top_k=2048, q_start=62000),
+    # ragged W and two sequences at different offsets
+    dict(B=2, S=600, W=12000, r=4, top_k=1000, q_start=[50000, 20000]),
+    # compress rate 1: rows from 1 to 8192 visible entries, trivial and scored items mixed
+    dict(B=1, S=8192, W=8192, r=1, top_k=2048),
+]
+
+
+@pytest.mark.parametrize("ci", range(len(LONG)))
+def test_long_rows_one_kernel(ci):
+    """The fused kernel's long-row mode (one shared row, selected by the four
+    select warps as one team) against the oracle, with and without the score
+    copy; the workspace is the staging ring, not [B,S,W] scores."""
+    c = dict(LONG[ci])
+    if isinstance(c.get("q_start"), int):
+        c["q_start"] = [c["q_start"]] * c["B"]
+    inp = _edge_inputs(dict(H=64, D=128, **c), seed=40 + ci)
+    wl = inp.wl
+    d = to_dev(inp)
+    p = csa.make_problem(d["q"], d["k"], d["w"], wl.scale, wl.compress_rate, wl.top_k)
+    # workspace: the staging ring (two items of four rows per CTA, at most 256
+    # CTAs) and the segment summaries -- independent of the score tensor's size
+    w_pad = (wl.W + 127) // 128 * 128
+    ring = min(wl.B * ((wl.S + 3) // 4), 256) * 2 * 4 * w_pad * 4
+    assert csa.workspace_size(p, 1) == (ring + 255) // 256 * 256 + wl.B * ((wl.S + 3) // 4) * 64
+    gs = gpu_scores(inp, d)
+    idx_p, _ = gpu_fused(inp, d, dbg=False)
+    idx_f, dbg = gpu_fused(inp, d, dbg=True)
+    assert_status_ok()
+    assert torch.equal(idx_p, idx_f)
+    assert torch.equal(dbg, gs)
+    g = gs.cpu().numpy()
+    gi = idx_p.cpu().numpy()
+    del gs, dbg
+    check_select_exact(g, gi, wl.top_k)
+    rng = np.random.default_rng(ci)
+    rows = np.unique(np.concatenate([[0, 1, wl.S - 1, wl.S // 2], rng.choice(wl.S, 40, replace=False)]))
+    ref = oracle_scores(inp, rows=rows)
+    check_scores(g[:, rows], ref)
+    check_select_vs_oracle(ref, gi[:, rows], wl.top_k)
+
+
+def test_long_rows_with_segments():
+    c = dict(B=2, S=520, W=9000, H=64, D=128, r=4, top_k=700, q_start=[40000, 36000])
+    for segs in ("packed", "scattered"):
+        inp = _edge_inputs(c, seed=50, segs=segs)
+        if segs == "packed":  # documents of the long rows: cut along the compressed entries
+            g = torch.Generator().manual_seed(51)
+            kv = torch.zeros(inp.wl.B, inp.wl.W, dtype=torch.int32)
+            for b in range(inp.wl.B):
+                for ct in torch.sort(torch.randint(1, inp.wl.W, (3,), generator=g)).values.tolist():
+                    kv[b, ct:] += 1
+            inp.kv_seg = kv
+            inp.q_seg = torch.full((inp.wl.B, inp.wl.S), 3, dtype=torch.int32)
+            inp.q_seg[:, : inp.wl.S // 2] = 2
+        _check_all(inp)
