@@ -450,27 +450,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool ok = mbar_wait(bars + Bq::acc_full, ac & 1u, ctl);
       tc_fence_after();
       ++ac;
+      // the whole row in registers first: the accumulator goes back to the
+      // accumulate issuer before any store (the stores of 32 different rows
+      // per instruction throttle, and the next pair's first product waits)
+      float v[4][32];
+      if (ok) {
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        float va[32], vb[32];
-        if (ok) {
-          tmem_ld32_start(t_acc + 64u * half, va);
-          tmem_ld32_start(t_acc + 64u * half + 32u, vb);
-          tmem_wait32(va);
-          tmem_wait32(vb);
-        }
-        if (half == 1) {
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bars + Bq::acc_empty);
-        }
-        if (ok && row_ok) {
+        for (int c = 0; c < 4; ++c) tmem_ld32_start(t_acc + 32u * c, v[c]);
 #pragma unroll
-          for (int i = 0; i < 8; ++i) d4[16 * half + i] = make_float4(va[4 * i], va[4 * i + 1], va[4 * i + 2], va[4 * i + 3]);
+        for (int c = 0; c < 4; ++c) tmem_wait32(v[c]);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bars + Bq::acc_empty);
+      if (ok && row_ok) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
 #pragma unroll
           for (int i = 0; i < 8; ++i)
-            d4[16 * half + 8 + i] = make_float4(vb[4 * i], vb[4 * i + 1], vb[4 * i + 2], vb[4 * i + 3]);
-        }
+            d4[8 * c + i] = make_float4(v[c][4 * i], v[c][4 * i + 1], v[c][4 * i + 2], v[c][4 * i + 3]);
       }
     }
   }
@@ -799,28 +797,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       ++ac;
       float* dst = p.dk + ((size_t)d.b * p.W + t) * kBD;
+      // the whole row in registers, the accumulator released, then the adds
+      float v[4][32];
+      if (ok) {
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        float va[32], vb[32];
-        if (ok) {
-          tmem_ld32_start(t_acc + 64u * half, va);
-          tmem_ld32_start(t_acc + 64u * half + 32u, vb);
-          tmem_wait32(va);
-          tmem_wait32(vb);
-        }
-        if (half == 1) {
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bars + Bk::acc_empty);
-        }
-        if (ok && t < p.W) {
-          float* d0 = dst + 64 * half;
+        for (int c = 0; c < 4; ++c) tmem_ld32_start(t_acc + 32u * c, v[c]);
 #pragma unroll
-          for (int i = 0; i < 8; ++i) red_add_f32x4(d0 + 4 * i, va[4 * i], va[4 * i + 1], va[4 * i + 2], va[4 * i + 3]);
+        for (int c = 0; c < 4; ++c) tmem_wait32(v[c]);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bars + Bk::acc_empty);
+      if (ok && t < p.W) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
 #pragma unroll
           for (int i = 0; i < 8; ++i)
-            red_add_f32x4(d0 + 32 + 4 * i, vb[4 * i], vb[4 * i + 1], vb[4 * i + 2], vb[4 * i + 3]);
-        }
+            red_add_f32x4(dst + 32 * c + 4 * i, v[c][4 * i], v[c][4 * i + 1], v[c][4 * i + 2], v[c][4 * i + 3]);
       }
     }
   }
