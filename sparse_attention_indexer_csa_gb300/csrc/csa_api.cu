@@ -200,6 +200,9 @@ csa_status run_index_kernel(const csa_problem* p, bool fused, const void* q, con
   kp.S = p->S;
   kp.W = p->W;
   kp.r = p->compress_rate;
+  kp.r_shift = -1;
+  for (int sh = 0; sh < 31; ++sh)
+    if ((1 << sh) == p->compress_rate) kp.r_shift = sh;
   kp.K = p->top_k;
   kp.scale = p->scale;
   kp.w_f32 = (p->w_dtype == CSA_F32) ? 1 : 0;
@@ -390,6 +393,9 @@ csa_status csa_index_backward(const csa_problem* p, const void* q, const void* k
   bp.S = p->S;
   bp.W = p->W;
   bp.r = p->compress_rate;
+  bp.r_shift = -1;
+  for (int sh = 0; sh < 31; ++sh)
+    if ((1 << sh) == p->compress_rate) bp.r_shift = sh;
   bp.n_pairs = (int)n_pairs;
   bp.n_items = (int)((long long)p->B * n_pairs);
   bp.n_tiles = (p->W + kTileT - 1) / kTileT;

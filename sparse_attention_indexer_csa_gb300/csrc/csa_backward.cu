@@ -114,12 +114,18 @@ struct DkBars {
 
 // ----------------------------------------------------------------- shared helpers
 // Visible-entry bound of row s of batch b (future mask): entries t < thr.
+// A shift replaces the division when the compress rate is a power of two;
+// without offsets the position fits 32 bits.
 __device__ __forceinline__ int row_thr(const BwdParams& p, int b, int s) {
   if (s >= p.S) return 0;
-  const long long qs0 = p.q_start ? (long long)p.q_start[b] : 0ll;
-  long long tv = (qs0 + s + 1) / p.r;
-  tv = tv < 0 ? 0 : (tv > p.W ? p.W : tv);
-  return (int)tv;
+  if (p.q_start == nullptr) {
+    const int tv = p.r_shift >= 0 ? ((s + 1) >> p.r_shift) : (s + 1) / p.r;
+    return tv > p.W ? p.W : tv;
+  }
+  const long long pos1 = (long long)p.q_start[b] + s + 1;
+  if (pos1 <= 0) return 0;
+  const long long tv = p.r_shift >= 0 ? (pos1 >> p.r_shift) : pos1 / p.r;
+  return tv > p.W ? p.W : (int)tv;
 }
 
 // Operand forms of the two products (M = 128, N = 128, eight K-steps of 16):
@@ -153,21 +159,42 @@ __device__ __forceinline__ void drain_waits(uint64_t* full_bars, int nbuf, uint3
 }
 
 // ======================================================================= dq
-// Item `it` of the dq kernel: batch and pair, the longest pairs (latest rows)
-// first so the static round-robin over the CTAs stays balanced.
+// Items of the dq kernel: item it is batch it % B and pair n_pairs-1 - it / B,
+// the longest pairs (latest rows) first so the static round-robin over the
+// CTAs stays balanced.  A CTA walks items it = blockIdx.x + k * gridDim.x
+// with the quotient and remainder kept as running counters (no division per
+// item in the issuing threads).
 struct DqItem {
   int b, s0, thr0, thr1, T;
 };
-__device__ __forceinline__ DqItem dq_item(const BwdParams& p, int it) {
-  DqItem d;
-  d.b = it % p.B;
-  const int pair = p.n_pairs - 1 - it / p.B;
-  d.s0 = 2 * pair;
-  d.thr0 = row_thr(p, d.b, d.s0);
-  d.thr1 = row_thr(p, d.b, d.s0 + 1);
-  d.T = (max(d.thr0, d.thr1) + kTileT - 1) / kTileT;
-  return d;
-}
+struct DqWalk {
+  int it, b, q, gq, gr;
+  __device__ explicit DqWalk(const BwdParams& p) : it((int)blockIdx.x) {
+    gq = (int)gridDim.x / p.B;
+    gr = (int)gridDim.x - gq * p.B;
+    q = it / p.B;
+    b = it - q * p.B;
+  }
+  __device__ bool more(const BwdParams& p) const { return it < p.n_items; }
+  __device__ void next(const BwdParams& p) {
+    it += (int)gridDim.x;
+    q += gq;
+    b += gr;
+    if (b >= p.B) {
+      b -= p.B;
+      ++q;
+    }
+  }
+  __device__ DqItem item(const BwdParams& p) const {
+    DqItem d;
+    d.b = b;
+    d.s0 = 2 * (p.n_pairs - 1 - q);
+    d.thr0 = row_thr(p, b, d.s0);
+    d.thr1 = row_thr(p, b, d.s0 + 1);
+    d.T = (max(d.thr0, d.thr1) + kTileT - 1) / kTileT;
+    return d;
+  }
+};
 
 __global__ void __launch_bounds__(kThreads, 1)
     csa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
@@ -221,8 +248,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {  // ---------------------------------------------- TMA producer
       const uint64_t q_pol = l2_policy_evict_first(), k_pol = l2_policy_evict_last();
       uint32_t qc = 0, kc = 0;
-      for (int it = blockIdx.x; it < p.n_items; it += gridDim.x) {
-        const DqItem d = dq_item(p, it);
+      for (DqWalk wk(p); wk.more(p); wk.next(p)) {
+        const DqItem d = wk.item(p);
         if (d.T == 0) continue;
         const int qb = qc % kQBufDq;
         if (mbar_wait(bars + Bq::q_empty + qb, ((qc / kQBufDq) & 1u) ^ 1u, ctl)) {
@@ -257,8 +284,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t kd0 = smem_desc_kmajor(smem_u32(base + DQ_OFF_K), 128);
       uint32_t qb = 0, qph = 0, kst = 0, kph = 0, xb = 0, xph = 0, n = 0;
       bool alive = true;
-      for (int it = blockIdx.x; it < p.n_items; it += gridDim.x) {
-        const DqItem d = dq_item(p, it);
+      for (DqWalk wk(p); wk.more(p); wk.next(p)) {
+        const DqItem d = wk.item(p);
         if (d.T == 0) continue;
         alive = alive && mbar_wait_u32(bar0 + 8u * (Bq::q_full + qb), qph, ctl);
         const uint64_t qd = qd0 + (uint64_t)(qb * (kBlk >> 4));
@@ -309,8 +336,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     float* gbuf = reinterpret_cast<float*>(base + DQ_OFF_G) + e * 128;
     float* dwx = reinterpret_cast<float*>(base + DQ_OFF_DW);
     uint32_t n = 0, ic = 0;
-    for (int it = blockIdx.x; it < p.n_items; it += gridDim.x, ++ic) {
-      const DqItem d = dq_item(p, it);
+    for (DqWalk wk(p); wk.more(p); wk.next(p), ++ic) {
+      const DqItem d = wk.item(p);
       const int s = d.s0 + j;
       const bool row_ok = s < p.S;
       const int thr = j ? d.thr1 : d.thr0;
@@ -398,8 +425,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t km0 = smem_desc_mn_sw128(smem_u32(base + DQ_OFF_K), kChunk, 1024u);
       uint32_t kst = 0, xb = 0, xph = 0, ac = 0;
       bool alive = true;
-      for (int it = blockIdx.x; it < p.n_items; it += gridDim.x) {
-        const DqItem d = dq_item(p, it);
+      for (DqWalk wk(p); wk.more(p); wk.next(p)) {
+        const DqItem d = wk.item(p);
         if (d.T == 0) continue;
         for (int tile = 0; tile < d.T; ++tile) {
           if (tile == 0) alive = alive && mbar_wait_u32(bar0 + 8u * Bq::acc_empty, (ac & 1u) ^ 1u, ctl);
@@ -435,8 +462,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int j = m >> 6, h = m & 63;
     const uint32_t t_acc = tmem + ((uint32_t)(quarter * 32) << 16) + kAccCol;
     uint32_t ac = 0;
-    for (int it = blockIdx.x; it < p.n_items; it += gridDim.x) {
-      const DqItem d = dq_item(p, it);
+    for (DqWalk wk(p); wk.more(p); wk.next(p)) {
+      const DqItem d = wk.item(p);
       const int s = d.s0 + j;
       const bool row_ok = s < p.S;
       float* dst = p.dq + (p.dq_seq_major ? (((size_t)d.b * p.S + s) * kBH + h) * kBD

@@ -66,6 +66,7 @@ cudaError_t take_status_gather(uint32_t* out, cudaStream_t stream);
 // items handed out through `counter`.
 struct BwdParams {
   int B, S, W, r;
+  int r_shift;      // log2(r) when r is a power of two, else -1
   int n_pairs;      // pairs of query rows per batch: (S + 1) / 2
   int n_items;      // dq kernel items: B * n_pairs
   int n_tiles;      // k tiles of 128 entries: ceil(W / 128)

@@ -52,6 +52,7 @@ struct SegInfo {
 
 struct KParams {
   int B, S, W, r, K;
+  int r_shift;  // log2(r) when r is a power of two, else -1
   float scale;
   int w_f32;
   const void* w;
@@ -210,8 +211,9 @@ __device__ __forceinline__ int item_rows(const KParams& p, int b, int s0, int (&
     const int s = s0 + j;
     long long tv = 0;
     if (s < p.S) {
-      tv = (qs0 + s + 1) / p.r;
-      tv = tv < 0 ? 0 : (tv > p.W ? p.W : tv);
+      const long long pos1 = qs0 + s + 1;
+      tv = pos1 <= 0 ? 0 : (p.r_shift >= 0 ? (pos1 >> p.r_shift) : pos1 / p.r);
+      tv = tv > p.W ? p.W : tv;
     }
     thr[j] = (int)tv;
     seg[j] = (p.q_seg != nullptr && s < p.S) ? p.q_seg[(size_t)b * p.S + s] : 0;
