@@ -246,11 +246,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     if (lane == 0) {  // ---------------------------------------------- TMA producer
+      // The q block of the next pair is requested right after the first k
+      // tile of the current one (its buffer was freed by the pair before),
+      // so its load overlaps the current pair's tiles.
       const uint64_t q_pol = l2_policy_evict_first(), k_pol = l2_policy_evict_last();
       uint32_t qc = 0, kc = 0;
-      for (DqWalk wk(p); wk.more(p); wk.next(p)) {
-        const DqItem d = wk.item(p);
-        if (d.T == 0) continue;
+      auto load_q = [&](const DqItem& d) {
         const int qb = qc % kQBufDq;
         if (mbar_wait(bars + Bq::q_empty + qb, ((qc / kQBufDq) & 1u) ^ 1u, ctl)) {
           uint8_t* dst = base + DQ_OFF_Q + qb * kBlk;
@@ -259,6 +260,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_4d_hint(dst + c * kChunk, &tmap_q, bars + Bq::q_full + qb, c * 64, 0, d.s0, d.b, q_pol);
         }
         ++qc;
+      };
+      // the next item that sees any tile
+      auto skip_empty = [&](DqWalk& w) {
+        while (w.more(p) && w.item(p).T == 0) w.next(p);
+      };
+      DqWalk wk(p);
+      skip_empty(wk);
+      if (wk.more(p)) load_q(wk.item(p));
+      while (wk.more(p)) {
+        const DqItem d = wk.item(p);
+        DqWalk nx = wk;
+        nx.next(p);
+        skip_empty(nx);
         for (int tile = 0; tile < d.T; ++tile, ++kc) {
           const int st = kc % kKStDq;
           if (mbar_wait(bars + Bq::k_empty + st, ((kc / kKStDq) & 1u) ^ 1u, ctl)) {
@@ -267,7 +281,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int c = 0; c < 2; ++c)
               tma_load_3d_hint(dst + c * kChunk, &tmap_k, bars + Bq::k_full + st, c * 64, tile * kTileT, d.b, k_pol);
           }
+          if (tile == 0 && nx.more(p)) load_q(nx.item(p));
         }
+        wk = nx;
       }
       drain_waits(bars + Bq::k_full, kKStDq, kc, ctl);
       drain_waits(bars + Bq::q_full, kQBufDq, qc, ctl);

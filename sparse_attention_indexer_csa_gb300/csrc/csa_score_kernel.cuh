@@ -117,6 +117,9 @@ struct Cfg {
   static constexpr int KSTAGES = (R == 1) ? 5 : 2;
   static constexpr int QBUF = FUSED ? 1 : 2;
   static constexpr int SLOTS = FUSED ? 6 : 4;      // item ring depth
+  // fused: the select warps' own ring of item descriptors, deeper than the
+  // item ring, so a selection that waits for its scores holds no item slot
+  static constexpr int SSLOTS = FUSED ? 16 : 0;
   static constexpr int EW = (R >= 2) ? 8 : 4;      // epilogue warps
   static constexpr int SW = FUSED ? R : 0;         // select warps (one row each)
   static constexpr int RW = (R >= 2) ? R / 2 : 1;  // rows per epilogue warp
@@ -133,10 +136,12 @@ struct Cfg {
   static constexpr uint32_t OFF_K = (OFF_Q + QBUF * QBYTES + 1023) & ~1023u;
   static constexpr uint32_t OFF_W = (OFF_K + KSTAGES * KBYTES + 1023) & ~1023u;
   static constexpr uint32_t OFF_DESC = OFF_W + SLOTS * R * H * 4;
-  static constexpr uint32_t OFF_BAR = (OFF_DESC + SLOTS * sizeof(ItemDesc<R>) + 15) & ~15u;
+  static constexpr uint32_t OFF_SDESC = OFF_DESC + SLOTS * sizeof(ItemDesc<R>);
+  static constexpr uint32_t OFF_BAR = (OFF_SDESC + SSLOTS * sizeof(ItemDesc<R>) + 15) & ~15u;
   // barriers: item_full[SLOTS], item_empty[SLOTS], q_full[QB], q_empty[QB], k_full[KS], k_empty[KS],
-  //           acc_full[2], acc_empty[2], drain, ring_full[2], ring_empty[2], copy_full
-  static constexpr int NBAR = 2 * SLOTS + 2 * QBUF + 2 * KSTAGES + 4 + 1 + 5;
+  //           acc_full[2], acc_empty[2], drain, ring_full[2], ring_empty[2], copy_full,
+  //           sel_full[SSLOTS], sel_empty[SSLOTS]
+  static constexpr int NBAR = 2 * SLOTS + 2 * QBUF + 2 * KSTAGES + 4 + 1 + 5 + 2 * SSLOTS;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;  // tmem base, abort flag
   static constexpr uint32_t OFF_STATS = (OFF_MISC + 16 + 15) & ~15u;  // RowStats[2][R]
   static constexpr uint32_t OFF_SCR = (OFF_STATS + 2 * R * sizeof(RowStats) + 15) & ~15u;
@@ -159,6 +164,9 @@ struct Smem {
   __device__ ItemDesc<C::R>* desc(int slot) const {
     return reinterpret_cast<ItemDesc<C::R>*>(base + C::OFF_DESC) + slot;
   }
+  __device__ ItemDesc<C::R>* sdesc(int slot) const {
+    return reinterpret_cast<ItemDesc<C::R>*>(base + C::OFF_SDESC) + slot;
+  }
   __device__ uint64_t* bar(int i) const { return reinterpret_cast<uint64_t*>(base + C::OFF_BAR) + i; }
   __device__ uint64_t* item_full(int s) const { return bar(s); }
   __device__ uint64_t* item_empty(int s) const { return bar(C::SLOTS + s); }
@@ -172,6 +180,8 @@ struct Smem {
   __device__ uint64_t* ring_full(int i) const { return bar(B2 + 5 + i); }
   __device__ uint64_t* ring_empty(int i) const { return bar(B2 + 7 + i); }
   __device__ uint64_t* copy_full() const { return bar(B2 + 9); }
+  __device__ uint64_t* sel_full(int s) const { return bar(B2 + 10 + s); }
+  __device__ uint64_t* sel_empty(int s) const { return bar(B2 + 10 + C::SSLOTS + s); }
   __device__ uint32_t* tmem_slot() const { return reinterpret_cast<uint32_t*>(base + C::OFF_MISC); }
   __device__ volatile uint32_t* abort_flag() const {
     return reinterpret_cast<volatile uint32_t*>(base + C::OFF_MISC + 4);
@@ -189,8 +199,7 @@ struct Smem {
 };
 
 // Item index -> (b, row block, chunk).  Row blocks run from the last (most
-// visible entries, most work) to the first so the static round-robin
-// assignment of items to CTAs stays balanced under the causal mask.
+// visible entries, most work) to the first, the batch index fastest.
 __device__ __forceinline__ void item_coords(const KParams& p, int item, int& b, int& rb, int& c) {
   c = item % p.n_chunks;
   const int rest = item / p.n_chunks;
@@ -198,13 +207,36 @@ __device__ __forceinline__ void item_coords(const KParams& p, int item, int& b, 
   rb = p.n_rb - 1 - rest / p.B;
 }
 
-// Scheduler warp `sw` (0 or 1) prepares the items with it % 2 == sw.
+// The items are dealt to the CTAs in rounds of gridDim.x.  Items of several
+// rows (ROT): in round k, CTA x takes item k * gridDim.x + (x + k) %
+// gridDim.x.  Each CTA's list keeps the longest-first order, and the
+// rotation moves a CTA to another batch every round; a plain round-robin
+// would give CTA x only batch x % B whenever B divides the grid, and batches
+// that differ (segments, offsets) would load the CTAs unevenly.  Single-row
+// items (decode chunks) carry equal work and take the plain round-robin.
+template <bool ROT>
+__device__ __forceinline__ int cta_item_count(const KParams& p) {
+  const int g = (int)gridDim.x, x = (int)blockIdx.x;
+  if constexpr (ROT) {
+    const int rounds = p.n_items / g, rem = p.n_items - rounds * g;
+    return rounds + (((x + rounds) % g) < rem ? 1 : 0);
+  } else {
+    return x < p.n_items ? (p.n_items - x + g - 1) / g : 0;
+  }
+}
+template <bool ROT>
+__device__ __forceinline__ int cta_item(int k) {
+  const int g = (int)gridDim.x;
+  return ROT ? k * g + ((int)blockIdx.x + k) % g : k * g + (int)blockIdx.x;
+}
+
 // Rows s0 .. s0+R-1 of batch b: each row's visible bound min(W, (pos+1)/r)
 // under the future mask (0 for rows past S) and its segment id (0 without
 // segments); returns the largest bound.
+// Visible bound min(W, (pos+1)/r) of rows s0 .. s0+R-1 of a sequence that
+// starts at position qs0 (0 for rows past S); returns the largest.
 template <int R>
-__device__ __forceinline__ int item_rows(const KParams& p, int b, int s0, int (&thr)[R], int (&seg)[R]) {
-  const long long qs0 = p.q_start ? (long long)p.q_start[b] : 0ll;
+__device__ __forceinline__ int row_bounds(const KParams& p, long long qs0, int s0, int (&thr)[R]) {
   int thr_max = 0;
 #pragma unroll
   for (int j = 0; j < R; ++j) {
@@ -216,10 +248,19 @@ __device__ __forceinline__ int item_rows(const KParams& p, int b, int s0, int (&
       tv = tv > p.W ? p.W : tv;
     }
     thr[j] = (int)tv;
-    seg[j] = (p.q_seg != nullptr && s < p.S) ? p.q_seg[(size_t)b * p.S + s] : 0;
     thr_max = max(thr_max, thr[j]);
   }
   return thr_max;
+}
+
+// Rows s0 .. s0+R-1 of batch b: each row's visible bound under the future
+// mask and its segment id (0 without segments); returns the largest bound.
+template <int R>
+__device__ __forceinline__ int item_rows(const KParams& p, int b, int s0, int (&thr)[R], int (&seg)[R]) {
+  const long long qs0 = p.q_start ? (long long)p.q_start[b] : 0ll;
+#pragma unroll
+  for (int j = 0; j < R; ++j) seg[j] = (p.q_seg != nullptr && s0 + j < p.S) ? p.q_seg[(size_t)b * p.S + s0 + j] : 0;
+  return row_bounds<R>(p, qs0, s0, thr);
 }
 
 // Segment scan of one item (a warp): over entries [e_lo, e_hi) of batch b,
@@ -297,95 +338,169 @@ __device__ void scan_segments(const KParams& p, int b, int e_lo, int e_hi, const
   }
 }
 
+// Item `it` of this CTA's list.  Fused: the items alternate from both ends of
+// the list (longest rows first, shortest last), so the cheap trivial items
+// are interleaved with scored ones instead of leaving the tensor cores idle
+// at the end.
+template <class C>
+__device__ __forceinline__ void sched_coords(const KParams& p, int it, int n_mine, int& b, int& rb, int& c) {
+  if constexpr (C::FUSED) {
+    const int jj = (it & 1) ? (n_mine - 1 - (it >> 1)) : (it >> 1);
+    item_coords(p, cta_item<(C::R > 1)>(jj), b, rb, c);
+  } else {
+    item_coords(p, cta_item<(C::R > 1)>(it), b, rb, c);
+  }
+}
+
+template <int R>
+__device__ __forceinline__ void write_desc(ItemDesc<R>* d, int b, int s0, int t_lo, int t_hi, int c_lo, int c_hi,
+                                           int trivial, const int (&thr)[R], const int (&seg)[R],
+                                           const int (&nvis)[R], const int (&tfirst)[R], const int (&contig)[R]) {
+  d->b = b;
+  d->s0 = s0;
+  d->t_lo = t_lo;
+  d->t_hi = t_hi;
+  d->c_lo = c_lo;
+  d->c_hi = c_hi;
+  d->trivial = trivial;
+#pragma unroll
+  for (int j = 0; j < R; ++j) {
+    d->thr[j] = thr[j];
+    d->seg[j] = seg[j];
+    d->nvis[j] = nvis[j];
+    d->tfirst[j] = tfirst[j];
+    d->contig[j] = contig[j];
+  }
+}
+
+// Scheduler warp `sw` (0 or 1) prepares the items it = sw, sw + 2, ...: per
+// item the visible tile range, per-row thresholds / segment ids / visible
+// counts, the trivial flag, and the weights of scored items.  The global
+// reads of 32 items at a time are made at once, one item per lane (the
+// items' latencies overlap instead of adding up), and handed to the item
+// loop through shuffles.
 template <class C>
 __device__ void run_scheduler(const KParams& p, const Smem<C>& sm, const WaitCtl& ctl, int sw) {
   constexpr int R = C::R, H = C::H;
+  constexpr int NWL = (R * H + 31) / 32;  // weights per lane
+  static_assert(R <= 4, "a segment summary covers four rows");
   const uint32_t lane = lane_id();
   const bool segs = p.q_seg != nullptr;
-  int it = 0;
-  for (int item = blockIdx.x; item < p.n_items; item += gridDim.x, ++it) {
-    if ((it & 1) != sw) continue;
-    const int slot = it % C::SLOTS;
-    mbar_wait(sm.item_empty(slot), ((it / C::SLOTS) & 1) ^ 1, ctl);
-    int b, rb, c;
-    if constexpr (C::FUSED) {
-      // the CTA's items alternate from both ends of its list (longest rows
-      // first, shortest last), so the cheap trivial items are interleaved
-      // with scored ones instead of leaving the tensor cores idle at the end
-      const int n_mine = (p.n_items - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
-      const int jj = (it & 1) ? (n_mine - 1 - (it >> 1)) : (it >> 1);
-      item_coords(p, (int)blockIdx.x + jj * (int)gridDim.x, b, rb, c);
-    } else {
-      item_coords(p, item, b, rb, c);
-    }
-    const int s0 = rb * R;
-    int thr[R], seg[R], nvis[R], tfirst[R], contig[R];
-    const int thr_max = item_rows<R>(p, b, s0, thr, seg);
-    const int c_lo = c * p.chunk_tiles;
-    const int c_hi = min(p.n_tiles, c_lo + p.chunk_tiles);
-    int t_lo = c_lo, t_hi = c_lo;
-    if (!segs) {
+  const bool pre = p.seginfo != nullptr;  // scanned ahead by csa_segscan_kernel (whole-row items)
+  const int n_mine = cta_item_count<(C::R > 1)>(p);
+  for (int it0 = sw; it0 < n_mine; it0 += 64) {
+    // lane l fetches item it0 + 2l
+    const int my_it = it0 + 2 * (int)lane;
+    int b_l = 0, rb_l = 0, c_l = 0;
+    long long qs_l = 0;
+    int seg_l[R];
+    SegInfo si_l{};
+#pragma unroll
+    for (int j = 0; j < R; ++j) seg_l[j] = 0;
+    if (my_it < n_mine) {
+      sched_coords<C>(p, my_it, n_mine, b_l, rb_l, c_l);
+      if (p.q_start != nullptr) qs_l = p.q_start[b_l];
+      if (segs) {
+#pragma unroll
+        for (int j = 0; j < R; ++j)
+          if (rb_l * R + j < p.S) seg_l[j] = p.q_seg[(size_t)b_l * p.S + rb_l * R + j];
+      }
+      if (pre) si_l = p.seginfo[(size_t)b_l * p.n_rb + rb_l];
+      // the weight rows of the item into L2: the item loop reads them from
+      // there if the item needs scores (a few hundred bytes per item)
+      const size_t esz = p.w_f32 ? 4 : 2;
 #pragma unroll
       for (int j = 0; j < R; ++j) {
-        nvis[j] = max(0, min(thr[j], c_hi * kTileT) - c_lo * kTileT);
-        tfirst[j] = c_lo * kTileT;
-        contig[j] = 1;
+        const int s = rb_l * R + j;
+        if (s < p.S) {
+          const char* a = static_cast<const char*>(p.w) + ((size_t)b_l * p.w_sb + (size_t)s * p.w_ss) * esz;
+          prefetch_l2(a);
+          prefetch_l2(a + H * esz - 1);
+        }
       }
-      t_hi = max(c_lo, min(c_hi, (thr_max + kTileT - 1) / kTileT));
-    } else if (p.seginfo != nullptr) {  // scanned ahead by csa_segscan_kernel (whole-row items)
-      const SegInfo& si = p.seginfo[(size_t)b * p.n_rb + rb];
+    }
+    const int cnt = min(32, (n_mine - it0 + 1) / 2);
+    for (int k = 0; k < cnt; ++k) {
+      const int it = it0 + 2 * k;
+      const int b = __shfl_sync(0xFFFFFFFFu, b_l, k);
+      const int rb = __shfl_sync(0xFFFFFFFFu, rb_l, k);
+      const int c = __shfl_sync(0xFFFFFFFFu, c_l, k);
+      const long long qs0 = __shfl_sync(0xFFFFFFFFu, qs_l, k);
+      const int s0 = rb * R;
+      int thr[R], seg[R], nvis[R], tfirst[R], contig[R];
 #pragma unroll
-      for (int j = 0; j < R; ++j) {
-        nvis[j] = si.nvis[j];
-        tfirst[j] = si.tfirst[j];
-        contig[j] = si.contig[j];
-      }
-      t_lo = si.t_lo;
-      t_hi = si.t_hi;
-    } else {
-      scan_segments<R>(p, b, c_lo * kTileT, min(c_hi * kTileT, thr_max), thr, seg, nvis, tfirst, contig, t_lo, t_hi);
-    }
-    int trivial = 0;
-    if (C::FUSED && p.scores == nullptr) {
-      trivial = 1;
+      for (int j = 0; j < R; ++j) seg[j] = __shfl_sync(0xFFFFFFFFu, seg_l[j], k);
+      const int thr_max = row_bounds<R>(p, qs0, s0, thr);
+      const int c_lo = c * p.chunk_tiles;
+      const int c_hi = min(p.n_tiles, c_lo + p.chunk_tiles);
+      int t_lo = c_lo, t_hi = c_lo;
+      if (!segs) {
 #pragma unroll
-      for (int j = 0; j < R; ++j) trivial &= (nvis[j] <= p.K) ? 1 : 0;
-      if (trivial) t_hi = t_lo;
-    }
-    // stage the weights (fp32) of the item's rows; rows past S get 0 (an item
-    // whose rows keep every visible entry computes no score and needs none)
-    float* ws = sm.w(slot);
-    for (int i = (int)lane; i < (trivial ? 0 : R * H); i += 32) {
-      const int j = i / H, h = i % H;
-      const int s = s0 + j;
-      float v = 0.f;
-      if (s < p.S) {
-        const size_t off = (size_t)b * p.w_sb + (size_t)s * p.w_ss + h;
-        v = p.w_f32 ? reinterpret_cast<const float*>(p.w)[off]
-                    : __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p.w)[off]);
-      }
-      ws[i] = v;
-    }
-    if (lane == 0) {
-      ItemDesc<R>* d = sm.desc(slot);
-      d->b = b;
-      d->s0 = s0;
-      d->t_lo = t_lo;
-      d->t_hi = t_hi;
-      d->c_lo = c_lo;
-      d->c_hi = c_hi;
-      d->trivial = trivial;
+        for (int j = 0; j < R; ++j) {
+          nvis[j] = max(0, min(thr[j], c_hi * kTileT) - c_lo * kTileT);
+          tfirst[j] = c_lo * kTileT;
+          contig[j] = 1;
+        }
+        t_hi = max(c_lo, min(c_hi, (thr_max + kTileT - 1) / kTileT));
+      } else if (pre) {
 #pragma unroll
-      for (int j = 0; j < R; ++j) {
-        d->thr[j] = thr[j];
-        d->seg[j] = seg[j];
-        d->nvis[j] = nvis[j];
-        d->tfirst[j] = tfirst[j];
-        d->contig[j] = contig[j];
+        for (int j = 0; j < R; ++j) {
+          nvis[j] = __shfl_sync(0xFFFFFFFFu, si_l.nvis[j], k);
+          tfirst[j] = __shfl_sync(0xFFFFFFFFu, si_l.tfirst[j], k);
+          contig[j] = __shfl_sync(0xFFFFFFFFu, si_l.contig[j], k);
+        }
+        t_lo = __shfl_sync(0xFFFFFFFFu, si_l.t_lo, k);
+        t_hi = __shfl_sync(0xFFFFFFFFu, si_l.t_hi, k);
+      } else {
+        scan_segments<R>(p, b, c_lo * kTileT, min(c_hi * kTileT, thr_max), thr, seg, nvis, tfirst, contig, t_lo,
+                         t_hi);
       }
+      int trivial = 0;
+      if (C::FUSED && p.scores == nullptr) {
+        trivial = 1;
+#pragma unroll
+        for (int j = 0; j < R; ++j) trivial &= (nvis[j] <= p.K) ? 1 : 0;
+        if (trivial) t_hi = t_lo;
+      }
+      // the weights (fp32) of a scored item's rows, every load in flight
+      // before the first store; rows past S get 0 (an item whose rows keep
+      // every visible entry computes no score and needs none)
+      float wv[NWL];
+#pragma unroll
+      for (int u = 0; u < NWL; ++u) {
+        const int i = (int)lane + 32 * u;
+        const int j = i / H, h = i % H;
+        const int s = s0 + j;
+        float v = 0.f;
+        if (!trivial && i < R * H && s < p.S) {
+          const size_t off = (size_t)b * p.w_sb + (size_t)s * p.w_ss + h;
+          v = p.w_f32 ? reinterpret_cast<const float*>(p.w)[off]
+                      : __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p.w)[off]);
+        }
+        wv[u] = v;
+      }
+      const int slot = it % C::SLOTS;
+      mbar_wait(sm.item_empty(slot), ((it / C::SLOTS) & 1) ^ 1, ctl);
+      if (!trivial) {
+        float* ws = sm.w(slot);
+#pragma unroll
+        for (int u = 0; u < NWL; ++u) {
+          const int i = (int)lane + 32 * u;
+          if (i < R * H) ws[i] = wv[u];
+        }
+      }
+      if (lane == 0) write_desc<R>(sm.desc(slot), b, s0, t_lo, t_hi, c_lo, c_hi, trivial, thr, seg, nvis, tfirst, contig);
+      if constexpr (C::FUSED) {
+        const int ss = it % C::SSLOTS;
+        mbar_wait(sm.sel_empty(ss), ((it / C::SSLOTS) & 1) ^ 1, ctl);
+        if (lane == 1)
+          write_desc<R>(sm.sdesc(ss), b, s0, t_lo, t_hi, c_lo, c_hi, trivial, thr, seg, nvis, tfirst, contig);
+        __syncwarp();
+        if (lane == 1) mbar_arrive(sm.sel_full(ss));
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(sm.item_full(slot));
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(sm.item_full(slot));
   }
 }
 
@@ -398,14 +513,37 @@ __device__ void run_producer(const KParams& p, const Smem<C>& sm, const WaitCtl&
   // should not push the scores of the selection pass out of L2
   const uint64_t q_pol = l2_policy_evict_first();
   const uint64_t k_pol = (C::R == 1) ? l2_policy_evict_first() : l2_policy_evict_last();
-  int it = 0;
-  for (int item = blockIdx.x; item < p.n_items; item += gridDim.x, ++it) {
+  const int n_mine = cta_item_count<(C::R > 1)>(p);
+  // Row-block items already posted to the item ring are looked at ahead of
+  // their turn, and the q block of each one that needs scores is prefetched
+  // into L2, so its load into the q buffer (which waits for the previous
+  // item's products) comes from L2.  `look` is the next item to look at.
+  int look = 1;
+  auto look_ahead = [&](int it) {
+    if constexpr (C::R > 1) {
+      look = max(look, it + 1);
+      const int lim = min(n_mine, it + C::SLOTS);
+      for (; look < lim; ++look) {
+        const int sl = look % C::SLOTS;
+        if (!mbar_test_wait(sm.item_full(sl), (look / C::SLOTS) & 1)) break;
+        const ItemDesc<C::R>* da = sm.desc(sl);
+        if (da->t_hi > da->t_lo) {
+#pragma unroll
+          for (int c = 0; c < C::NKC; ++c) tma_prefetch_4d(tq, c * C::KC, 0, da->s0, da->b);
+        }
+      }
+    }
+  };
+  for (int it = 0; it < n_mine; ++it) {
     const int slot = it % C::SLOTS;
     const bool ok_item = mbar_wait(sm.item_full(slot), (it / C::SLOTS) & 1, ctl);
     const ItemDesc<C::R>* d = sm.desc(slot);
     const int b = d->b, s0 = d->s0, t_lo = d->t_lo, t_hi = d->t_hi;
     mbar_arrive(sm.item_empty(slot));
-    if (!ok_item || t_hi <= t_lo) continue;
+    if (!ok_item || t_hi <= t_lo) {
+      if (ok_item) look_ahead(it);
+      continue;
+    }
     const int qb = qcount % C::QBUF;
     if (mbar_wait(sm.q_empty(qb), ((qcount / C::QBUF) & 1) ^ 1, ctl)) {
       mbar_arrive_expect_tx(sm.q_full(qb), C::QBYTES);
@@ -414,6 +552,7 @@ __device__ void run_producer(const KParams& p, const Smem<C>& sm, const WaitCtl&
         tma_load_4d_hint(sm.q(qb) + c * C::QCHUNK, tq, sm.q_full(qb), c * C::KC, 0, s0, b, q_pol);
     }
     ++qcount;
+    look_ahead(it);
     for (int tile = t_lo; tile < t_hi; ++tile) {
       const int st = kcount % C::KSTAGES;
       if (mbar_wait(sm.k_empty(st), ((kcount / C::KSTAGES) & 1) ^ 1, ctl)) {
@@ -423,6 +562,7 @@ __device__ void run_producer(const KParams& p, const Smem<C>& sm, const WaitCtl&
           tma_load_3d_hint(sm.k(st) + c * C::KCHUNK, tk, sm.k_full(st), c * C::KC, tile * kTileT, b, k_pol);
       }
       ++kcount;
+      look_ahead(it);
     }
   }
   // make sure no copy is still landing in shared memory when the CTA exits
@@ -441,8 +581,8 @@ __device__ void run_producer(const KParams& p, const Smem<C>& sm, const WaitCtl&
 template <class C>
 __device__ void run_mma(const KParams& p, const Smem<C>& sm, const WaitCtl& ctl, uint32_t tmem_base) {
   uint32_t kcount = 0, qcount = 0, acount = 0;
-  int it = 0;
-  for (int item = blockIdx.x; item < p.n_items; item += gridDim.x, ++it) {
+  const int n_mine = cta_item_count<(C::R > 1)>(p);
+  for (int it = 0; it < n_mine; ++it) {
     const int slot = it % C::SLOTS;
     const bool ok_item = mbar_wait(sm.item_full(slot), (it / C::SLOTS) & 1, ctl);
     const ItemDesc<C::R>* d = sm.desc(slot);
@@ -582,8 +722,8 @@ __device__ void run_epilogue(const KParams& p, const Smem<C>& sm, const WaitCtl&
   const uint32_t t_lane = tmem_base + ((uint32_t)(quarter * 32) << 16);
   uint32_t acount = 0, nt = 0;
   const uint64_t sc_pol = l2_policy_evict_last();
-  int it = 0;
-  for (int item = blockIdx.x; item < p.n_items; item += gridDim.x, ++it) {
+  const int n_mine = cta_item_count<(C::R > 1)>(p);
+  for (int it = 0; it < n_mine; ++it) {
     const int slot = it % C::SLOTS;
     mbar_wait(sm.item_full(slot), (it / C::SLOTS) & 1, ctl);
     const ItemDesc<R>* d = sm.desc(slot);
@@ -694,20 +834,22 @@ __device__ void run_selector(const KParams& p, const Smem<C>& sm, const WaitCtl&
   const Team<32> team{0u, lane};
   FusedRowScratch* fs = sm.scratch(j);
   uint32_t nt = 0;
-  int it = 0;
-  for (int item = blockIdx.x; item < p.n_items; item += gridDim.x, ++it) {
-    const int slot = it % C::SLOTS;
-    mbar_wait(sm.item_full(slot), (it / C::SLOTS) & 1, ctl);
-    const ItemDesc<R>* d = sm.desc(slot);
+  const int n_mine = cta_item_count<(C::R > 1)>(p);
+  for (int it = 0; it < n_mine; ++it) {
+    const int ss = it % C::SSLOTS;
+    mbar_wait(sm.sel_full(ss), (it / C::SSLOTS) & 1, ctl);
+    const ItemDesc<R>* d = sm.sdesc(ss);
     const int b = d->b, s0 = d->s0, s = s0 + j;
+    const int trivial = d->trivial, t_lo = d->t_lo, t_hi = d->t_hi;
+    const int nvis = d->nvis[j], tfirst = d->tfirst[j], contig = d->contig[j], thr = d->thr[j], seg = d->seg[j];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(sm.sel_empty(ss));
     int32_t* out = p.idx + ((size_t)b * p.S + s) * p.K;
-    if (d->trivial) {
+    if (trivial) {
       if (s < p.S)
-        write_visible_set<32>(out, p.K, d->nvis[j], d->tfirst[j], d->contig[j], d->thr[j], d->seg[j],
-                              p.kv_seg + (size_t)b * p.W, &fs->sc, team);
+        write_visible_set<32>(out, p.K, nvis, tfirst, contig, thr, seg, p.kv_seg + (size_t)b * p.W, &fs->sc, team);
     } else {
       const int rs = (int)(nt & 1u);
-      const int t_lo = d->t_lo, t_hi = d->t_hi;
       const int e0 = t_lo * kTileT;
       const uint32_t row_bytes = (uint32_t)(t_hi - t_lo) * kTileT * 4u;
       mbar_wait(sm.ring_full(rs), (nt >> 1) & 1u, ctl);
@@ -736,8 +878,6 @@ __device__ void run_selector(const KParams& p, const Smem<C>& sm, const WaitCtl&
       named_bar_sync(kSelBar, 32 * R);  // the shared rows may be refilled
       ++nt;
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(sm.item_empty(slot));
   }
 }
 
@@ -756,20 +896,23 @@ __device__ void run_selector_long(const KParams& p, const Smem<C>& sm, const Wai
   LongRowScratch* ls = sm.long_scratch();
   float* srow = sm.srow(0, p.w_pad);
   uint32_t nt = 0, nc = 0;  // scored items, row copies
-  int it = 0;
-  for (int item = blockIdx.x; item < p.n_items; item += gridDim.x, ++it) {
-    const int slot = it % C::SLOTS;
-    mbar_wait(sm.item_full(slot), (it / C::SLOTS) & 1, ctl);
-    const ItemDesc<R>* d = sm.desc(slot);
+  const int n_mine = cta_item_count<(C::R > 1)>(p);
+  for (int it = 0; it < n_mine; ++it) {
+    const int ss = it % C::SSLOTS;
+    mbar_wait(sm.sel_full(ss), (it / C::SSLOTS) & 1, ctl);
+    const ItemDesc<R>* d = sm.sdesc(ss);
     const int b = d->b, s0 = d->s0;
-    if (d->trivial) {
+    const int trivial = d->trivial, t_lo = d->t_lo, t_hi = d->t_hi;
+    const int nvis = d->nvis[j], tfirst = d->tfirst[j], contig = d->contig[j], thr = d->thr[j], seg = d->seg[j];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(sm.sel_empty(ss));
+    if (trivial) {
       const int s = s0 + j;
       if (s < p.S)
-        write_visible_set<32>(p.idx + ((size_t)b * p.S + s) * p.K, p.K, d->nvis[j], d->tfirst[j], d->contig[j],
-                              d->thr[j], d->seg[j], p.kv_seg + (size_t)b * p.W, &ls->sc[j], wteam);
+        write_visible_set<32>(p.idx + ((size_t)b * p.S + s) * p.K, p.K, nvis, tfirst, contig, thr, seg,
+                              p.kv_seg + (size_t)b * p.W, &ls->sc[j], wteam);
     } else {
       const int rs = (int)(nt & 1u);
-      const int t_lo = d->t_lo, t_hi = d->t_hi;
       const int e0 = t_lo * kTileT, n = (t_hi - t_lo) * kTileT;
       const uint32_t row_bytes = (uint32_t)n * 4u;
       mbar_wait(sm.ring_full(rs), (nt >> 1) & 1u, ctl);
@@ -803,8 +946,6 @@ __device__ void run_selector_long(const KParams& p, const Smem<C>& sm, const Wai
       }
       ++nt;
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(sm.item_empty(slot));
   }
 }
 
@@ -821,7 +962,11 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::SLOTS; ++s) {
       mbar_init(sm.item_full(s), 1);
-      mbar_init(sm.item_empty(s), 2 + C::EW + C::SW);
+      mbar_init(sm.item_empty(s), 2 + C::EW);  // producer, MMA issuer, epilogue warps
+    }
+    for (int s = 0; s < C::SSLOTS; ++s) {
+      mbar_init(sm.sel_full(s), 1);
+      mbar_init(sm.sel_empty(s), C::SW);
     }
     for (int i = 0; i < C::QBUF; ++i) {
       mbar_init(sm.q_full(i), 1);
