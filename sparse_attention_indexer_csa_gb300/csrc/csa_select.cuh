@@ -65,6 +65,22 @@ struct BinScratch {
   uint32_t keep[MAXW];
 };
 
+// Bin of a score in a row whose visible scores span [lo, hi] (lo < hi): a
+// monotone map onto 0 .. NB-1.  A saturating fma takes x onto [0, 1]; a
+// second fma scales that to [0, NB-1] and adds 2^23, which rounds it to an
+// integer read from the mantissa.  Each step is a monotone function of its
+// input, so bins are ordered value intervals (not exactly equal in width),
+// and every finite x lands in range.
+struct BinMap {
+  float s, b, nb1;
+  __device__ BinMap(float lo, float span, int nb) : s(1.0f / span), b(-lo / span), nb1((float)(nb - 1)) {}
+  __device__ __forceinline__ uint32_t operator()(float x) const {
+    float y;
+    asm("fma.rn.sat.f32 %0, %1, %2, %3;" : "=f"(y) : "f"(x), "f"(s), "f"(b));
+    return __float_as_uint(fmaf(y, nb1, 8388608.0f)) - 0x4B000000u;
+  }
+};
+
 // Visible count and value range of one row.
 struct RowStats {
   uint32_t nvis;
@@ -265,9 +281,8 @@ __device__ __noinline__ void select_general(const float* row, int t0, int n, uin
 // Selection of one row whose scores live in shared memory at row[t0, t0+n):
 // t0 and n multiples of 128, row 16-byte aligned, entries past the row's end
 // hold -inf; the indices written are absolute entry numbers.  `st` holds the
-// row's visible count and value range.  The bin of x is
-// round(clamp(x*scale + bias, 0, NB-1)) read from the mantissa of that value
-// plus 2^23: a monotone map of x, identical in every pass.
+// row's visible count and value range.  The bin of x is BinMap: a monotone
+// map of x, identical in every pass.
 template <int NT, int NB, int CAP, int MAXW>
 __device__ void team_topk_row(float* row, int t0, int n, uint32_t K, const RowStats& st, int32_t* out,
                               BinScratch<NB, CAP, MAXW>* bs, SelectScratch* sc, const Team<NT>& team) {
@@ -294,10 +309,7 @@ __device__ void team_topk_row(float* row, int t0, int n, uint32_t K, const RowSt
     select_general<NT>(row, t0, n, K, 0u, 0u, true, out, sc, team.bar_id, team.tid);
     return;
   }
-  const float nb1 = (float)(NB - 1);
-  auto bin_of = [&](float x) -> uint32_t {  // in [0, NB-1] for any finite x
-    return __float_as_uint(fmaxf(fminf(fmaf(x, scale, bias), nb1), 0.0f) + 8388608.0f) - 0x4B000000u;
-  };
+  const BinMap bin_of(lo, span, NB);  // in [0, NB-1] for any finite x
   // shared-space addresses: entry e of the row's range at row_s + 4*e
   const uint32_t row_s = smem_u32(row + t0);
   const uint32_t hist_s = smem_u32(bs->hist), keep_s = smem_u32(bs->keep);

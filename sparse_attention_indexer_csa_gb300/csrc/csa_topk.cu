@@ -230,10 +230,7 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kClNT)
   const uint32_t lt_mask = (1u << lane) - 1u;
   const uint32_t row_s = smem_u32(row);
   if (binned) {
-    const float nb1 = (float)(NB - 1);
-    auto bin_of = [&](float x) -> uint32_t {
-      return __float_as_uint(fmaxf(fminf(fmaf(x, scale, bias), nb1), 0.0f) + 8388608.0f) - 0x4B000000u;
-    };
+    const BinMap bin_of(lo, span, NB);
     const uint32_t hist_s = smem_u32(cs->hist);
 #pragma unroll
     for (int j = 0; j < PER; ++j) cs->hist[tid * PER + j] = 0u;
