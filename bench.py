@@ -610,7 +610,8 @@ def side_leg(wl, dev, stream, steps=50, warmup=5):
         bf = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
         a = wk["flops_nontrivial"] / (ms * 1e-3) / 1e12
         out["roofline"] = {"bound": "tensor", "achieved": a, "peak": bf, "unit": "TFLOP/s", "frac": a / bf,
-                           "traffic": None, "peak_source": f"{peak_src} bf16_tflops",
+                           "traffic": measured_traffic(f"{wl.name}_seed{wl.seed}"),
+                           "peak_source": f"{peak_src} bf16_tflops",
                            "achieved_counts": "2*H*D per visible pair of rows with visible > top_k"}
     del q, k, w, qs, ks, st, idx, ws
     return out

@@ -268,6 +268,12 @@ __device__ __forceinline__ int item_rows(const KParams& p, int b, int s0, int (&
 // whether they form one contiguous run -- and the tiles [t_lo, t_hi) that
 // hold any of them (t_lo = t_hi when none does).  Segment ids are read with
 // 16-byte loads, four in flight per lane, when they are aligned.
+//
+// When the item's rows share one segment id (the usual case: four
+// consecutive rows of one document), entries below the smallest row bound
+// are visible to every row or to none, so that prefix takes one comparison
+// per entry; only the few entries between the rows' bounds are checked per
+// row.
 template <int R>
 __device__ void scan_segments(const KParams& p, int b, int e_lo, int e_hi, const int (&thr)[R], const int (&seg)[R],
                               int (&nvis)[R], int (&tfirst)[R], int (&contig)[R], int& t_lo, int& t_hi) {
@@ -281,7 +287,6 @@ __device__ void scan_segments(const KParams& p, int b, int e_lo, int e_hi, const
     tmx[j] = -1;
   }
   const int32_t* kv = p.kv_seg + (size_t)b * p.W;
-  const bool vec = ((reinterpret_cast<uintptr_t>(kv) & 15u) == 0) && (e_lo % 4 == 0);
   auto visit = [&](int t, int ks) {
 #pragma unroll
     for (int j = 0; j < R; ++j) {
@@ -293,30 +298,64 @@ __device__ void scan_segments(const KParams& p, int b, int e_lo, int e_hi, const
       }
     }
   };
-  if (vec) {
-    // four 16-byte loads in flight per lane per round (512 entries per warp)
-    for (int t0 = e_lo + 4 * (int)lane; t0 < e_hi; t0 += 512) {
-      int4 v4[4];
+  // calls f(t, kv[t]) for every entry of [lo, hi) this lane owns
+  auto scan = [&](int lo, int hi, auto&& f) {
+    const bool vec = ((reinterpret_cast<uintptr_t>(kv) & 15u) == 0) && (lo % 4 == 0);
+    if (vec) {
+      // four 16-byte loads in flight per lane per round (512 entries per warp)
+      for (int t0 = lo + 4 * (int)lane; t0 < hi; t0 += 512) {
+        int4 v4[4];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int t = t0 + 128 * u;
-        v4[u] = (t + 3 < e_hi) ? *reinterpret_cast<const int4*>(kv + t) : make_int4(0, 0, 0, 0);
-      }
+        for (int u = 0; u < 4; ++u) {
+          const int t = t0 + 128 * u;
+          v4[u] = (t + 3 < hi) ? *reinterpret_cast<const int4*>(kv + t) : make_int4(0, 0, 0, 0);
+        }
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int t = t0 + 128 * u;
-        if (t + 3 < e_hi) {
-          visit(t, v4[u].x);
-          visit(t + 1, v4[u].y);
-          visit(t + 2, v4[u].z);
-          visit(t + 3, v4[u].w);
-        } else {
-          for (int x = t; x < e_hi; ++x) visit(x, kv[x]);
+        for (int u = 0; u < 4; ++u) {
+          const int t = t0 + 128 * u;
+          if (t + 3 < hi) {
+            f(t, v4[u].x);
+            f(t + 1, v4[u].y);
+            f(t + 2, v4[u].z);
+            f(t + 3, v4[u].w);
+          } else {
+            for (int x = t; x < hi; ++x) f(x, kv[x]);
+          }
         }
       }
+    } else {
+      for (int t = lo + (int)lane; t < hi; t += 32) f(t, kv[t]);
     }
+  };
+  bool uni = true;
+  int ta = e_hi;  // smallest row bound (rows past S have bound 0 and id 0)
+#pragma unroll
+  for (int j = 0; j < R; ++j) {
+    uni = uni && seg[j] == seg[0];
+    ta = min(ta, thr[j]);
+  }
+  ta = max(ta, e_lo);
+  if (uni && ta > e_lo) {
+    // [e_lo, ta): every row's bound is at or above ta
+    const int sg = seg[0];
+    int c = 0, mn = 0x7FFFFFFF, mx = -1;
+    scan(e_lo, ta, [&](int t, int ks) {
+      const bool m = ks == sg;
+      c += m;
+      if (m) {
+        mn = min(mn, t);
+        mx = max(mx, t);
+      }
+    });
+#pragma unroll
+    for (int j = 0; j < R; ++j) {
+      cnt[j] = c;
+      tmn[j] = mn;
+      tmx[j] = mx;
+    }
+    for (int t = ta + (int)lane; t < e_hi; t += 32) visit(t, kv[t]);
   } else {
-    for (int t = e_lo + (int)lane; t < e_hi; t += 32) visit(t, kv[t]);
+    scan(e_lo, e_hi, visit);
   }
   int tmin = 0x7FFFFFFF, tmax = -1;
 #pragma unroll
