@@ -144,6 +144,42 @@ def test_full_size_fused_debug_scores():
     check_select_vs_oracle(ref, gi[:, rows], wl.top_k)
 
 
+@pytest.mark.parametrize("H,D,B,S,r,top_k,docs", [
+    (4, 32, 1, 65536, 32, 256, None),
+    (4, 32, 1, 65536, 32, 256, (3, 8)),
+    (64, 128, 3, 13312, 4, 1024, None),
+])
+def test_many_items_per_cta(H, D, B, S, r, top_k, docs):
+    """More than 64 items of four rows per CTA: the scheduler warps fetch the
+    descriptions of 32 items each at a time, so later fetch rounds run here.
+    The indices with and without the score copy agree, the oracle selector on
+    the copy gives them on every row, and sampled rows match the oracle's own
+    scores."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert B * ((S + 3) // 4) > 64 * sms
+    wl = Workload(name="many", B=B, S=S, W=S // r, H=H, D=D, compress_rate=r, top_k=top_k, w_dtype="bf16",
+                  sigma_w=1.0 / 8, scale=D ** -0.5, docs=docs, seed=11)
+    inp = make_inputs(wl)
+    d = to_dev(inp)
+    idx_dbg, dbg = gpu_fused(inp, d, dbg=True)
+    idx_p, _ = gpu_fused(inp, d, dbg=False)
+    assert_status_ok()
+    assert torch.equal(idx_dbg, idx_p)
+    g = dbg.cpu().numpy()
+    gi = idx_p.cpu().numpy()
+    del dbg
+    check_select_exact(g, gi, top_k)
+    for b in range(B):
+        segrow = None if inp.q_seg is None else inp.q_seg[b].numpy()
+        rows = _sample_rows(S, wl.W, r, top_k, segrow, n=256, seed=b)
+        sub = Inputs(wl.with_(B=1), inp.q[b:b + 1], inp.k[b:b + 1], inp.w[b:b + 1],
+                     None if inp.q_seg is None else inp.q_seg[b:b + 1],
+                     None if inp.kv_seg is None else inp.kv_seg[b:b + 1], None)
+        ref = oracle_scores(sub, rows=rows)
+        check_scores(g[b:b + 1, rows], ref)
+        check_select_vs_oracle(ref, gi[b:b + 1, rows], top_k)
+
+
 def test_decode_full():
     wl = WORKLOADS["decode_32k"]
     inp = make_inputs(wl)
