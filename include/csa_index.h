@@ -194,11 +194,17 @@ csa_status csa_index_fused_noalloc(const csa_problem* p, const void* q, const vo
  * pair of query rows, the other dk per tile of 128 entries and run of row
  * pairs, adding its partial sums into dk with fp32 atomics (so the last bits
  * of dk may differ from call to call); the [B,H,S,W] tensor and P never
- * reach HBM.  Needs `workspace`: csa_index_workspace_size(p, 2) bytes
- * (256; 16-byte aligned), a work counter the call resets.  dk is zeroed and
- * two kernels run on `stream`; the call returns once they are enqueued and
- * allocates nothing.  Supported: H = 64, D = 128, either q layout.
- * Added in ABI version 102; the workspace shrank to 256 bytes in 103.     */
+ * reach HBM.  With segment ids, a pre-pass summarises each item of four
+ * rows (the tiles holding entries visible to its rows, as for
+ * csa_index_fused) and the kernels skip the tiles, and the dk kernel the
+ * row pairs, that the segment mask leaves without a visible entry.  Needs
+ * `workspace`: csa_index_workspace_size(p, 2) bytes (256 + 64 per item of
+ * four rows, B * ceil(S/4) items; 16-byte aligned): a work counter the call
+ * resets, then the summaries.  dk is zeroed and the kernels run on
+ * `stream`; the call returns once they are enqueued and allocates nothing.
+ * Supported: H = 64, D = 128, either q layout.  Added in ABI version 102;
+ * the workspace shrank to 256 bytes in 103 and holds the segment summaries
+ * since 105.                                                              */
 csa_status csa_index_backward(const csa_problem* p, const void* q, const void* k, const void* w,
                               const int32_t* q_seg, const int32_t* kv_seg, const int64_t* q_start,
                               const float* g, float* dq, float* dk, float* dw, void* workspace,
@@ -223,7 +229,8 @@ csa_status csa_index_selftest_timeout(uint32_t timeout_us, void* stream);
 /* Static string for a status code. */
 const char* csa_status_string(csa_status s);
 
-/* ABI version (major * 100 + minor): 104 (strides in csa_problem). */
+/* ABI version (major * 100 + minor): 105 (backward workspace holds the
+ * segment summaries; 104: strides in csa_problem). */
 int32_t csa_index_abi_version(void);
 
 #ifdef __cplusplus

@@ -169,11 +169,13 @@ bool make_k_map(CUtensorMap* m, const csa_problem* p, const void* k) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Backward workspace: the dk kernel's item counter.
+// Backward workspace: the dk kernel's item counter (256 bytes), then the
+// segment summaries of the items of four rows (64 bytes each; written and
+// read only when segment ids are given).
 constexpr size_t kBwdWorkspace = 256;
 size_t backward_workspace_bytes(const csa_problem* p) {
   if (check_problem(p) != CSA_OK) return 0;
-  return kBwdWorkspace;
+  return kBwdWorkspace + (size_t)p->B * (size_t)((p->S + 3) / 4) * sizeof(SegInfo);
 }
 
 // Row pairs per dk item: 256, halved while the problem would give fewer than
@@ -416,7 +418,28 @@ csa_status csa_index_backward(const csa_problem* p, const void* q, const void* k
   bp.dk = dk;
   bp.dw = dw;
   bp.counter = static_cast<unsigned int*>(workspace);
+  bp.n_rb = (p->S + 3) / 4;
   bp.wait_ns = kWaitNs;
+  if (q_seg != nullptr) {
+    // segment summaries of the items of four rows, by the forward's pre-pass
+    SegInfo* si = reinterpret_cast<SegInfo*>(static_cast<uint8_t*>(workspace) + kBwdWorkspace);
+    KParams kp;
+    std::memset(&kp, 0, sizeof(kp));
+    kp.B = p->B;
+    kp.S = p->S;
+    kp.W = p->W;
+    kp.r = p->compress_rate;
+    kp.r_shift = bp.r_shift;
+    kp.q_seg = q_seg;
+    kp.kv_seg = kv_seg;
+    kp.q_start = q_start;
+    kp.n_rb = bp.n_rb;
+    kp.n_tiles = bp.n_tiles;
+    kp.n_chunks = 1;
+    kp.chunk_tiles = bp.n_tiles;
+    if (launch_segscan(kp, si, sms, static_cast<cudaStream_t>(stream)) != cudaSuccess) return CSA_ERR_CUDA;
+    bp.seginfo = si;
+  }
   if (launch_backward(tq, tk, bp, sms, static_cast<cudaStream_t>(stream)) != cudaSuccess) return CSA_ERR_CUDA;
   return CSA_OK;
 }
@@ -471,6 +494,6 @@ const char* csa_status_string(csa_status s) {
   return "unknown status";
 }
 
-int32_t csa_index_abi_version(void) { return 104; }
+int32_t csa_index_abi_version(void) { return 105; }
 
 }  // extern "C"

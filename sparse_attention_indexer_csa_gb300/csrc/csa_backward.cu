@@ -165,7 +165,8 @@ __device__ __forceinline__ void drain_waits(uint64_t* full_bars, int nbuf, uint3
 // with the quotient and remainder kept as running counters (no division per
 // item in the issuing threads).
 struct DqItem {
-  int b, s0, thr0, thr1, T;
+  int b, s0, thr0, thr1;
+  int t0, T;  // the pair's k tiles: t0 .. t0 + T - 1
 };
 struct DqWalk {
   int it, b, q, gq, gr;
@@ -192,6 +193,15 @@ struct DqWalk {
     d.thr0 = row_thr(p, b, d.s0);
     d.thr1 = row_thr(p, b, d.s0 + 1);
     d.T = (max(d.thr0, d.thr1) + kTileT - 1) / kTileT;
+    d.t0 = 0;
+    if (p.seginfo != nullptr) {
+      // with segment ids: only the tiles holding an entry visible to a row
+      // of the pair's item of four rows (its segment summary)
+      const SegInfo& si = p.seginfo[(size_t)b * p.n_rb + (d.s0 >> 2)];
+      const int hi = min(d.T, si.t_hi);
+      d.t0 = si.t_lo;
+      d.T = hi > si.t_lo ? hi - si.t_lo : 0;
+    }
     return d;
   }
 };
@@ -279,7 +289,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint8_t* dst = base + DQ_OFF_K + st * kBlk;
             mbar_arrive_expect_tx(bars + Bq::k_full + st, kBlk);
             for (int c = 0; c < 2; ++c)
-              tma_load_3d_hint(dst + c * kChunk, &tmap_k, bars + Bq::k_full + st, c * 64, tile * kTileT, d.b, k_pol);
+              tma_load_3d_hint(dst + c * kChunk, &tmap_k, bars + Bq::k_full + st, c * 64, (d.t0 + tile) * kTileT,
+                               d.b, k_pol);
           }
           if (tile == 0 && nx.more(p)) load_q(nx.item(p));
         }
@@ -372,7 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         float gv[2];
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
-          const int t = tile * kTileT + hf * 64 + 2 * (int)lane + u;
+          const int t = (d.t0 + tile) * kTileT + hf * 64 + 2 * (int)lane + u;
           bool vis = row_ok && t < thr;
           if (vis && segs) vis = p.kv_seg[(size_t)d.b * p.W + t] == seg;
           gv[u] = vis ? p.g[((size_t)d.b * p.S + s) * p.W + t] : 0.f;
@@ -533,6 +544,34 @@ __device__ __forceinline__ int dk_first_pair(const BwdParams& p, int b, int tile
   return (int)(s_first / 2);
 }
 
+// With segment ids (a warp): narrows the pairs [lo, hi) of a dk item to the
+// span from the first to the last pair whose item of four rows holds a
+// visible entry in `tile` (its segment summary); lo = hi when none does.
+// Pairs inside the span that see nothing form P = 0.
+__device__ __forceinline__ void dk_trim(const BwdParams& p, int b, int tile, int& lo, int& hi) {
+  const uint32_t lane = lane_id();
+  int first = hi, last = lo - 1;
+  for (int base = lo; base < hi; base += 32) {
+    const int pr = base + (int)lane;
+    bool in = false;
+    if (pr < hi) {
+      const SegInfo& si = p.seginfo[(size_t)b * p.n_rb + (pr >> 1)];
+      in = tile >= si.t_lo && tile < si.t_hi;
+    }
+    const uint32_t m = __ballot_sync(0xFFFFFFFFu, in);
+    if (m != 0u) {
+      first = min(first, base + __ffs((int)m) - 1);
+      last = max(last, base + 31 - __clz((int)m));
+    }
+  }
+  if (last < first) {
+    hi = lo;
+  } else {
+    lo = first;
+    hi = last + 1;
+  }
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     csa_bwd_dk_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                       const BwdParams p) {
@@ -595,51 +634,66 @@ __global__ void __launch_bounds__(kThreads, 1)
     return ok && out.b >= 0;
   };
 
-  if (warp == 0) {
-    if (lane == 0) {  // ------------------------------- scheduler + TMA producer
-      const uint64_t q_pol = l2_policy_evict_last(), k_pol = l2_policy_evict_last();
-      const long long n_raw = (long long)p.B * p.n_chunks * p.n_tiles;
-      uint32_t ic = 0, qc = 0;
-      // raw item x -> (b, chunk, tile), tile fastest: the items of one chunk
-      // of rows (the same q blocks) are taken one after another
-      unsigned int x = atomicAdd(p.counter, 1u);
-      while (!*abort_flag) {
-        DkItem d{-1, 0, 0, 0};
-        while ((long long)x < n_raw) {
-          const int tile = (int)(x % (unsigned)p.n_tiles);
-          const int rest = (int)(x / (unsigned)p.n_tiles);
-          const int chunk = rest % p.n_chunks, b = rest / p.n_chunks;
-          x = atomicAdd(p.counter, 1u);  // the next one, while this one is set up
-          const int lo = max(chunk * p.chunk_pairs, dk_first_pair(p, b, tile));
-          const int hi = min((chunk + 1) * p.chunk_pairs, p.n_pairs);
-          if (lo < hi) {
-            d = DkItem{b, tile, lo, hi};
-            break;
-          }
+  if (warp == 0) {  // ------------------------------- scheduler + TMA producer
+    // Lane 0 takes items from the counter, publishes them and issues the
+    // copies; with segment ids the whole warp first trims each item's pairs.
+    const uint64_t q_pol = l2_policy_evict_last(), k_pol = l2_policy_evict_last();
+    const long long n_raw = (long long)p.B * p.n_chunks * p.n_tiles;
+    uint32_t ic = 0, qc = 0;
+    // raw item x -> (b, chunk, tile), tile fastest: the items of one chunk
+    // of rows (the same q blocks) are taken one after another
+    unsigned int x = 0;
+    if (lane == 0) x = atomicAdd(p.counter, 1u);
+    x = __shfl_sync(0xFFFFFFFFu, x, 0);
+    while (__shfl_sync(0xFFFFFFFFu, *abort_flag, 0) == 0u) {  // lane 0's reading, for the whole warp
+      DkItem d{-1, 0, 0, 0};
+      while ((long long)x < n_raw) {
+        const int tile = (int)(x % (unsigned)p.n_tiles);
+        const int rest = (int)(x / (unsigned)p.n_tiles);
+        const int chunk = rest % p.n_chunks, b = rest / p.n_chunks;
+        unsigned int xn = 0;
+        if (lane == 0) xn = atomicAdd(p.counter, 1u);  // the next one, while this one is set up
+        int lo = max(chunk * p.chunk_pairs, dk_first_pair(p, b, tile));
+        int hi = min((chunk + 1) * p.chunk_pairs, p.n_pairs);
+        if (lo < hi && p.seginfo != nullptr) dk_trim(p, b, tile, lo, hi);
+        x = __shfl_sync(0xFFFFFFFFu, xn, 0);
+        if (lo < hi) {
+          d = DkItem{b, tile, lo, hi};
+          break;
         }
+      }
+      uint32_t go = 0u;
+      if (lane == 0) {
         const int slot = ic % kItemSlots;
-        if (!mbar_wait(bars + Bk::item_empty + slot, ((ic / kItemSlots) & 1u) ^ 1u, ctl)) break;
-        slots[slot] = d;
-        mbar_arrive(bars + Bk::item_full + slot);
-        if (d.b < 0) break;
-        const int kb = ic % kKtBufDk;
-        if (mbar_wait(bars + Bk::kt_empty + kb, ((ic / kKtBufDk) & 1u) ^ 1u, ctl)) {
-          uint8_t* dst = base + DK_OFF_KT + kb * kBlk;
-          mbar_arrive_expect_tx(bars + Bk::kt_full + kb, kBlk);
-          for (int c = 0; c < 2; ++c)
-            tma_load_3d_hint(dst + c * kChunk, &tmap_k, bars + Bk::kt_full + kb, c * 64, d.tile * kTileT, d.b, k_pol);
+        if (mbar_wait(bars + Bk::item_empty + slot, ((ic / kItemSlots) & 1u) ^ 1u, ctl)) {
+          slots[slot] = d;
+          mbar_arrive(bars + Bk::item_full + slot);
+          go = d.b >= 0 ? 1u : 0u;
         }
-        ++ic;
-        for (int pr = d.p_lo; pr < d.p_hi; ++pr, ++qc) {
-          const int st = qc % kQStDk;
-          if (mbar_wait(bars + Bk::q_empty + st, ((qc / kQStDk) & 1u) ^ 1u, ctl)) {
-            uint8_t* dst = base + DK_OFF_Q + st * kBlk;
-            mbar_arrive_expect_tx(bars + Bk::q_full + st, kBlk);
+        if (go) {
+          const int kb = ic % kKtBufDk;
+          if (mbar_wait(bars + Bk::kt_empty + kb, ((ic / kKtBufDk) & 1u) ^ 1u, ctl)) {
+            uint8_t* dst = base + DK_OFF_KT + kb * kBlk;
+            mbar_arrive_expect_tx(bars + Bk::kt_full + kb, kBlk);
             for (int c = 0; c < 2; ++c)
-              tma_load_4d_hint(dst + c * kChunk, &tmap_q, bars + Bk::q_full + st, c * 64, 0, 2 * pr, d.b, q_pol);
+              tma_load_3d_hint(dst + c * kChunk, &tmap_k, bars + Bk::kt_full + kb, c * 64, d.tile * kTileT, d.b,
+                               k_pol);
+          }
+          ++ic;
+          for (int pr = d.p_lo; pr < d.p_hi; ++pr, ++qc) {
+            const int st = qc % kQStDk;
+            if (mbar_wait(bars + Bk::q_empty + st, ((qc / kQStDk) & 1u) ^ 1u, ctl)) {
+              uint8_t* dst = base + DK_OFF_Q + st * kBlk;
+              mbar_arrive_expect_tx(bars + Bk::q_full + st, kBlk);
+              for (int c = 0; c < 2; ++c)
+                tma_load_4d_hint(dst + c * kChunk, &tmap_q, bars + Bk::q_full + st, c * 64, 0, 2 * pr, d.b, q_pol);
+            }
           }
         }
       }
+      if (__shfl_sync(0xFFFFFFFFu, go, 0) == 0u) break;
+    }
+    if (lane == 0) {
       drain_waits(bars + Bk::q_full, kQStDk, qc, ctl);
       drain_waits(bars + Bk::kt_full, kKtBufDk, ic, ctl);
     }

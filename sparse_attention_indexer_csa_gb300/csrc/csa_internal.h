@@ -85,6 +85,8 @@ struct BwdParams {
   float* dk;          // [B,W,D] fp32 (zeroed, then accumulated)
   float* dw;          // [B,S,H] fp32
   unsigned int* counter;  // dk item counter (device memory, zeroed before the launch)
+  const SegInfo* seginfo;  // with segment ids: [B][n_rb] summaries of items of four rows, else null
+  int n_rb;                // items of four rows per batch: ceil(S / 4)
   unsigned long long wait_ns;
 };
 // Enqueues the whole backward on `stream` (two memsets, two kernels).

@@ -39,7 +39,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_abi_version_and_strings(lib):
-    assert lib.csa_index_abi_version() == 104
+    assert lib.csa_index_abi_version() == 105
     for s in range(6):
         assert abi.status_string(s)
     assert abi.status_string(99) == "unknown status"
@@ -137,9 +137,11 @@ def _bwd(lib, p, g=FAKE, dq=FAKE, dk=FAKE, dw=FAKE, ws=FAKE, nbytes=1 << 40, q=F
 
 
 def test_backward_workspace_size():
-    # the dk kernel's work counter only: P never leaves the SM
-    for kw in (dict(S=16, W=4), dict(S=16384, W=4096), dict(S=5, W=300), dict(S=16384, W=32768)):
-        assert abi.workspace_size(_p(**kw), 2) == 256
+    # the dk kernel's work counter, then a 64-byte segment summary per item of
+    # four rows: P never leaves the SM
+    for kw in (dict(S=16, W=4), dict(S=16384, W=4096), dict(S=5, W=300), dict(S=16384, W=32768, B=3)):
+        pp = _p(**kw)
+        assert abi.workspace_size(pp, 2) == 256 + pp.B * ((pp.S + 3) // 4) * 64
     assert abi.workspace_size(_p(B=0), 2) == 0
 
 

@@ -131,6 +131,8 @@ def test_hand_example_exact_in_64_heads():
     dict(B=2, S=301, W=100, seed=1),                          # odd rows (last pair half empty), W % 128 != 0
     dict(B=1, S=256, W=300, seed=2, w_dtype="f32"),
     dict(B=2, S=200, W=64, seed=3, docs=(2, 4)),             # packed documents: segment mask
+    dict(B=2, S=2048, W=512, seed=11, docs=(3, 8)),          # documents over several tiles: tiles and pairs skipped
+    dict(B=2, S=1536, W=900, seed=12, docs=(2, 5), q_start=2000),  # documents with offset rows
     dict(B=2, S=40, W=700, seed=4, q_start=600),             # offset rows: every chunk spans all entries
     dict(B=3, S=1, W=1000, seed=8, q_start=5000),            # one row per sequence (decode shape)
     dict(B=1, S=100, W=6000, seed=9, q_start=30000),         # rows longer than 4096 entries (47 tiles)
