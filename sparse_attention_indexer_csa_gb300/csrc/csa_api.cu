@@ -235,6 +235,8 @@ csa_status run_index_kernel(const csa_problem* p, bool fused, const void* q, con
     // segment ids scanned once per item across the whole GPU, ahead of the kernel
     if (launch_segscan(kp, seginfo, sms, stream) != cudaSuccess) return CSA_ERR_CUDA;
     kp.seginfo = seginfo;
+    // packed documents: the kernel's document mode
+    kc.docs = fused && !kc.long_rows && p->H == 64 && p->D == 128;
   }
   if (launch_index_kernel(kc, tq, tk, kp, grid, stream) != cudaSuccess) return CSA_ERR_CUDA;
   return CSA_OK;

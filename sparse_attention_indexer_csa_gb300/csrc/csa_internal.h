@@ -40,6 +40,7 @@ struct KernelChoice {
   int H, D, R;
   bool fused;
   bool long_rows = false;  // fused with rows of 4097..16384 entries
+  bool docs = false;       // fused with segment summaries: the document mode (H = 64, D = 128)
 };
 
 // Launch the persistent score (or fused score + selection) kernel.

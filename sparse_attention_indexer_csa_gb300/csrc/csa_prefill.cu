@@ -1,7 +1,8 @@
 // csa_prefill.cu -- instantiations of the persistent indexer kernel and their
 // launcher: R = 4 query rows per item (prefill score, fused score +
-// selection, and its long-row mode for rows of up to 16384 entries) and
-// R = 1 with tile chunks (single-row decode scores).
+// selection, its long-row mode for rows of up to 16384 entries and its
+// document mode for packed documents) and R = 1 with tile chunks
+// (single-row decode scores).
 #include "csa_internal.h"
 
 namespace csa {
@@ -55,10 +56,15 @@ size_t smem_cfg(int w_pad) {
 
 }  // namespace
 
-#define CSA_DISPATCH(H_, D_, R_, F_, CALL)                                       \
-  if (kc.H == H_ && kc.D == D_ && kc.R == R_ && kc.fused == F_ && !kc.long_rows) { \
-    using C = Cfg<H_, D_, R_, F_>;                                               \
-    CALL;                                                                        \
+#define CSA_DISPATCH(H_, D_, R_, F_, CALL)                                                     \
+  if (kc.H == H_ && kc.D == D_ && kc.R == R_ && kc.fused == F_ && !kc.long_rows && !kc.docs) { \
+    using C = Cfg<H_, D_, R_, F_>;                                                             \
+    CALL;                                                                                      \
+  }
+#define CSA_DISPATCH_DOCS(H_, D_, CALL)                                             \
+  if (kc.H == H_ && kc.D == D_ && kc.R == 4 && kc.fused && !kc.long_rows && kc.docs) { \
+    using C = Cfg<H_, D_, 4, true, false, true>;                                    \
+    CALL;                                                                           \
   }
 #define CSA_DISPATCH_LONG(H_, D_, CALL)                                        \
   if (kc.H == H_ && kc.D == D_ && kc.R == 4 && kc.fused && kc.long_rows) {     \
@@ -71,6 +77,7 @@ cudaError_t launch_index_kernel(const KernelChoice& kc, const CUtensorMap& tq, c
   CSA_DISPATCH(64, 128, 4, false, return launch_cfg<C>(tq, tk, p, grid, stream))
   CSA_DISPATCH(64, 128, 4, true, return launch_cfg<C>(tq, tk, p, grid, stream))
   CSA_DISPATCH_LONG(64, 128, return launch_cfg<C>(tq, tk, p, grid, stream))
+  CSA_DISPATCH_DOCS(64, 128, return launch_cfg<C>(tq, tk, p, grid, stream))
   CSA_DISPATCH(64, 128, 1, false, return launch_cfg<C>(tq, tk, p, grid, stream))
   CSA_DISPATCH(4, 32, 4, false, return launch_cfg<C>(tq, tk, p, grid, stream))
   CSA_DISPATCH(4, 32, 4, true, return launch_cfg<C>(tq, tk, p, grid, stream))
@@ -81,6 +88,7 @@ size_t index_kernel_smem(const KernelChoice& kc, int w_pad) {
   CSA_DISPATCH(64, 128, 4, false, return smem_cfg<C>(w_pad))
   CSA_DISPATCH(64, 128, 4, true, return smem_cfg<C>(w_pad))
   CSA_DISPATCH_LONG(64, 128, return smem_cfg<C>(w_pad))
+  CSA_DISPATCH_DOCS(64, 128, return smem_cfg<C>(w_pad))
   CSA_DISPATCH(64, 128, 1, false, return smem_cfg<C>(w_pad))
   CSA_DISPATCH(4, 32, 4, false, return smem_cfg<C>(w_pad))
   CSA_DISPATCH(4, 32, 4, true, return smem_cfg<C>(w_pad))

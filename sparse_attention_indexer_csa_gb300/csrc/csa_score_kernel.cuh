@@ -102,11 +102,15 @@ constexpr uint32_t pow2_cols(uint32_t n) {
   return c;
 }
 
-template <int H_, int D_, int R_, bool FUSED_, bool LONG_ = false>
+template <int H_, int D_, int R_, bool FUSED_, bool LONG_ = false, bool DOCS_ = false>
 struct Cfg {
   static constexpr int H = H_, D = D_, R = R_;
   static constexpr bool FUSED = FUSED_;
   static constexpr bool LONG = LONG_;  // fused, rows of 4097..16384 entries
+  // fused with segment summaries (packed documents): the scheduler posts only
+  // the items that need scores to the item ring, which ends with a marker
+  static constexpr bool DOCS = DOCS_;
+  static_assert(!DOCS || (FUSED && !LONG), "the document mode is the fused kernel's");
   static_assert(!LONG || (FUSED && R_ == 4), "long-row mode is the fused four-row kernel");
   static constexpr int N = R * H;
   static_assert(N % 16 == 0 && N >= 16 && N <= 256, "UMMA N must be 16..256 in steps of 16");
@@ -543,6 +547,189 @@ __device__ void run_scheduler(const KParams& p, const Smem<C>& sm, const WaitCtl
   }
 }
 
+// Scheduler of the document mode (C::DOCS).  The warps describe the CTA's items in order: the visible
+// tile range, per-row thresholds / segment ids / visible counts and the
+// trivial flag, and post them to two rings, each ending with an end marker
+// on the item ring:
+//  * the select warps' ring takes every item; item it is posted by warp
+//    it % 2 (its slot's parity is the item's, so every slot has one writer
+//    and is written in order);
+//  * the item ring (producer, MMA issuer, epilogue) takes, with segment ids
+//    (packed documents, where most items are trivial), only the items that
+//    need scores, all posted by warp 0 in order, so trivial items never hold
+//    a slot the tensor-core roles wait behind; without segment ids (scored
+//    and trivial items alternate) every item, posted by warp it % 2.
+// The global reads of 32 items are made at once, one item per lane, and
+// handed to the item loop through shuffles.
+template <class C>
+__device__ void run_scheduler_docs(const KParams& p, const Smem<C>& sm, const WaitCtl& ctl, int sw) {
+  constexpr int R = C::R, H = C::H;
+  constexpr int NWL = (R * H + 31) / 32;  // weights per lane
+  static_assert(R <= 4, "a segment summary covers four rows");
+  static_assert(!C::FUSED || C::SSLOTS % 2 == 0, "select slots alternate between the two scheduler warps");
+  const uint32_t lane = lane_id();
+  const bool to_items = sw == 0;
+  const bool segs = p.q_seg != nullptr;
+  const bool pre = p.seginfo != nullptr;  // scanned ahead by csa_segscan_kernel (whole-row items)
+  const bool can_trivial = C::FUSED && p.scores == nullptr;
+  const bool only_scored = can_trivial && pre;  // item ring: the items that need scores, from warp 0
+  const int n_mine = cta_item_count<(C::R > 1)>(p);
+  int posted = 0;  // item-ring entries written so far (only_scored: warp 0)
+  for (int it0 = 0; it0 < n_mine; it0 += 32) {
+    // lane l fetches item it0 + l
+    const int my_it = it0 + (int)lane;
+    int b_l = 0, rb_l = 0, c_l = 0;
+    long long qs_l = 0;
+    int seg_l[R];
+    SegInfo si_l{};
+    bool triv_l = false;  // known trivial (then only the select ring takes the item)
+#pragma unroll
+    for (int j = 0; j < R; ++j) seg_l[j] = 0;
+    if (my_it < n_mine) {
+      sched_coords<C>(p, my_it, n_mine, b_l, rb_l, c_l);
+      if (p.q_start != nullptr) qs_l = p.q_start[b_l];
+      if (segs) {
+#pragma unroll
+        for (int j = 0; j < R; ++j)
+          if (rb_l * R + j < p.S) seg_l[j] = p.q_seg[(size_t)b_l * p.S + rb_l * R + j];
+      }
+      if (pre) si_l = p.seginfo[(size_t)b_l * p.n_rb + rb_l];
+      // whether the item keeps every visible entry, where a lane can tell
+      // on its own (without segment ids, or from the segment summary)
+      if (can_trivial && (!segs || pre)) {
+        int thr[R];
+        row_bounds<R>(p, qs_l, rb_l * R, thr);
+        const int c_lo = c_l * p.chunk_tiles, c_hi = min(p.n_tiles, c_lo + p.chunk_tiles);
+        bool all = true;
+#pragma unroll
+        for (int j = 0; j < R; ++j) {
+          const int nv = segs ? si_l.nvis[j] : max(0, min(thr[j], c_hi * kTileT) - c_lo * kTileT);
+          all = all && nv <= p.K;
+        }
+        triv_l = all;
+      }
+      if (only_scored ? to_items : ((my_it & 1) == sw)) {
+        // the weight rows of the item into L2: the item loop reads them from
+        // there if the item needs scores (a few hundred bytes per item)
+        const size_t esz = p.w_f32 ? 4 : 2;
+#pragma unroll
+        for (int j = 0; j < R; ++j) {
+          const int s = rb_l * R + j;
+          if (s < p.S) {
+            const char* a = static_cast<const char*>(p.w) + ((size_t)b_l * p.w_sb + (size_t)s * p.w_ss) * esz;
+            prefetch_l2(a);
+            prefetch_l2(a + H * esz - 1);
+          }
+        }
+      }
+    }
+    const int cnt = min(32, n_mine - it0);
+    for (int k = 0; k < cnt; ++k) {
+      const int it = it0 + k;
+      const bool triv_k = __shfl_sync(0xFFFFFFFFu, triv_l, k);
+      // a warp describes its own items; with only_scored, warp 0 also the
+      // other warp's items unless they are known to keep every visible entry
+      if ((it & 1) != sw && (!only_scored || !to_items || triv_k)) continue;
+      const int b = __shfl_sync(0xFFFFFFFFu, b_l, k);
+      const int rb = __shfl_sync(0xFFFFFFFFu, rb_l, k);
+      const int c = __shfl_sync(0xFFFFFFFFu, c_l, k);
+      const long long qs0 = __shfl_sync(0xFFFFFFFFu, qs_l, k);
+      const int s0 = rb * R;
+      int thr[R], seg[R], nvis[R], tfirst[R], contig[R];
+#pragma unroll
+      for (int j = 0; j < R; ++j) seg[j] = __shfl_sync(0xFFFFFFFFu, seg_l[j], k);
+      const int thr_max = row_bounds<R>(p, qs0, s0, thr);
+      const int c_lo = c * p.chunk_tiles;
+      const int c_hi = min(p.n_tiles, c_lo + p.chunk_tiles);
+      int t_lo = c_lo, t_hi = c_lo;
+      if (!segs) {
+#pragma unroll
+        for (int j = 0; j < R; ++j) {
+          nvis[j] = max(0, min(thr[j], c_hi * kTileT) - c_lo * kTileT);
+          tfirst[j] = c_lo * kTileT;
+          contig[j] = 1;
+        }
+        t_hi = max(c_lo, min(c_hi, (thr_max + kTileT - 1) / kTileT));
+      } else if (pre) {
+#pragma unroll
+        for (int j = 0; j < R; ++j) {
+          nvis[j] = __shfl_sync(0xFFFFFFFFu, si_l.nvis[j], k);
+          tfirst[j] = __shfl_sync(0xFFFFFFFFu, si_l.tfirst[j], k);
+          contig[j] = __shfl_sync(0xFFFFFFFFu, si_l.contig[j], k);
+        }
+        t_lo = __shfl_sync(0xFFFFFFFFu, si_l.t_lo, k);
+        t_hi = __shfl_sync(0xFFFFFFFFu, si_l.t_hi, k);
+      } else {
+        scan_segments<R>(p, b, c_lo * kTileT, min(c_hi * kTileT, thr_max), thr, seg, nvis, tfirst, contig, t_lo,
+                         t_hi);
+      }
+      int trivial = 0;
+      if (can_trivial) {
+        trivial = 1;
+#pragma unroll
+        for (int j = 0; j < R; ++j) trivial &= (nvis[j] <= p.K) ? 1 : 0;
+        if (trivial) t_hi = t_lo;
+      }
+      if constexpr (C::FUSED) {
+        if ((it & 1) == sw) {  // the select ring
+          const int ss = it % C::SSLOTS;
+          mbar_wait(sm.sel_empty(ss), ((it / C::SSLOTS) & 1) ^ 1, ctl);
+          if (lane == 0)
+            write_desc<R>(sm.sdesc(ss), b, s0, t_lo, t_hi, c_lo, c_hi, trivial, thr, seg, nvis, tfirst, contig);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(sm.sel_full(ss));
+        }
+      }
+      int ki;  // item-ring entry
+      if (only_scored) {
+        if (!to_items || trivial) continue;  // the select warps alone handle a trivial item
+        ki = posted++;
+      } else {
+        ki = it;  // this warp's own item, trivial or not
+      }
+      // the weights (fp32) of a scored item's rows, every load in flight
+      // before the first store; rows past S get 0
+      float wv[NWL];
+#pragma unroll
+      for (int u = 0; u < NWL; ++u) {
+        const int i = (int)lane + 32 * u;
+        const int j = i / H, h = i % H;
+        const int s = s0 + j;
+        float v = 0.f;
+        if (!trivial && i < R * H && s < p.S) {
+          const size_t off = (size_t)b * p.w_sb + (size_t)s * p.w_ss + h;
+          v = p.w_f32 ? reinterpret_cast<const float*>(p.w)[off]
+                      : __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p.w)[off]);
+        }
+        wv[u] = v;
+      }
+      const int slot = ki % C::SLOTS;
+      mbar_wait(sm.item_empty(slot), ((ki / C::SLOTS) & 1) ^ 1, ctl);
+      if (!trivial) {
+        float* ws = sm.w(slot);
+#pragma unroll
+        for (int u = 0; u < NWL; ++u) {
+          const int i = (int)lane + 32 * u;
+          if (i < R * H) ws[i] = wv[u];
+        }
+      }
+      if (lane == 0) write_desc<R>(sm.desc(slot), b, s0, t_lo, t_hi, c_lo, c_hi, trivial, thr, seg, nvis, tfirst, contig);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(sm.item_full(slot));
+    }
+  }
+  // end marker (b < 0) after the last item-ring entry: from warp 0 with
+  // only_scored, else from the warp whose parity the entry index has
+  const int end_at = only_scored ? posted : n_mine;
+  if (only_scored ? to_items : ((end_at & 1) == sw)) {
+    const int slot = end_at % C::SLOTS;
+    mbar_wait(sm.item_empty(slot), ((end_at / C::SLOTS) & 1) ^ 1, ctl);
+    if (lane == 0) sm.desc(slot)->b = -1;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(sm.item_full(slot));
+  }
+}
+
 template <class C>
 __device__ void run_producer(const KParams& p, const Smem<C>& sm, const WaitCtl& ctl, const CUtensorMap* tq,
                              const CUtensorMap* tk) {
@@ -552,7 +739,8 @@ __device__ void run_producer(const KParams& p, const Smem<C>& sm, const WaitCtl&
   // should not push the scores of the selection pass out of L2
   const uint64_t q_pol = l2_policy_evict_first();
   const uint64_t k_pol = (C::R == 1) ? l2_policy_evict_first() : l2_policy_evict_last();
-  const int n_mine = cta_item_count<(C::R > 1)>(p);
+  // document mode: the item ring until its end marker
+  const int n_mine = C::DOCS ? 0x7FFFFFFF : cta_item_count<(C::R > 1)>(p);
   // Row-block items already posted to the item ring are looked at ahead of
   // their turn, and the q block of each one that needs scores is prefetched
   // into L2, so its load into the q buffer (which waits for the previous
@@ -566,6 +754,7 @@ __device__ void run_producer(const KParams& p, const Smem<C>& sm, const WaitCtl&
         const int sl = look % C::SLOTS;
         if (!mbar_test_wait(sm.item_full(sl), (look / C::SLOTS) & 1)) break;
         const ItemDesc<C::R>* da = sm.desc(sl);
+        if (C::DOCS && da->b < 0) break;  // the end marker
         if (da->t_hi > da->t_lo) {
 #pragma unroll
           for (int c = 0; c < C::NKC; ++c) tma_prefetch_4d(tq, c * C::KC, 0, da->s0, da->b);
@@ -579,6 +768,7 @@ __device__ void run_producer(const KParams& p, const Smem<C>& sm, const WaitCtl&
     const ItemDesc<C::R>* d = sm.desc(slot);
     const int b = d->b, s0 = d->s0, t_lo = d->t_lo, t_hi = d->t_hi;
     mbar_arrive(sm.item_empty(slot));
+    if (C::DOCS && (!ok_item || b < 0)) break;
     if (!ok_item || t_hi <= t_lo) {
       if (ok_item) look_ahead(it);
       continue;
@@ -620,13 +810,16 @@ __device__ void run_producer(const KParams& p, const Smem<C>& sm, const WaitCtl&
 template <class C>
 __device__ void run_mma(const KParams& p, const Smem<C>& sm, const WaitCtl& ctl, uint32_t tmem_base) {
   uint32_t kcount = 0, qcount = 0, acount = 0;
-  const int n_mine = cta_item_count<(C::R > 1)>(p);
+  // document mode: the item ring until its end marker
+  const int n_mine = C::DOCS ? 0x7FFFFFFF : cta_item_count<(C::R > 1)>(p);
   for (int it = 0; it < n_mine; ++it) {
     const int slot = it % C::SLOTS;
     const bool ok_item = mbar_wait(sm.item_full(slot), (it / C::SLOTS) & 1, ctl);
     const ItemDesc<C::R>* d = sm.desc(slot);
     const int t_lo = d->t_lo, t_hi = d->t_hi;
+    const int b_mark = d->b;
     mbar_arrive(sm.item_empty(slot));
+    if (C::DOCS && (!ok_item || b_mark < 0)) break;
     if (!ok_item || t_hi <= t_lo) continue;
     const int qb = qcount % C::QBUF;
     const bool q_ok = mbar_wait(sm.q_full(qb), (qcount / C::QBUF) & 1, ctl);
@@ -761,11 +954,13 @@ __device__ void run_epilogue(const KParams& p, const Smem<C>& sm, const WaitCtl&
   const uint32_t t_lane = tmem_base + ((uint32_t)(quarter * 32) << 16);
   uint32_t acount = 0, nt = 0;
   const uint64_t sc_pol = l2_policy_evict_last();
-  const int n_mine = cta_item_count<(C::R > 1)>(p);
+  // document mode: the item ring until its end marker
+  const int n_mine = C::DOCS ? 0x7FFFFFFF : cta_item_count<(C::R > 1)>(p);
   for (int it = 0; it < n_mine; ++it) {
     const int slot = it % C::SLOTS;
-    mbar_wait(sm.item_full(slot), (it / C::SLOTS) & 1, ctl);
+    const bool ok_it = mbar_wait(sm.item_full(slot), (it / C::SLOTS) & 1, ctl);
     const ItemDesc<R>* d = sm.desc(slot);
+    if (C::DOCS && (!ok_it || d->b < 0)) break;
     const int b = d->b, s0 = d->s0, t_lo = d->t_lo, t_hi = d->t_hi, c_lo = d->c_lo, c_hi = d->c_hi;
     if (C::FUSED && d->trivial) {  // the select warps write the visible sets
       __syncwarp();
@@ -1053,7 +1248,10 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
   } else if (warp == 1) {
     if (lane == 0) run_mma<C>(p, sm, ctl, tmem_base);
   } else if (warp == 2 || warp == 3) {
-    run_scheduler<C>(p, sm, ctl, warp - 2);
+    if constexpr (C::DOCS)
+      run_scheduler_docs<C>(p, sm, ctl, warp - 2);
+    else
+      run_scheduler<C>(p, sm, ctl, warp - 2);
   } else if (warp < 4 + C::EW) {
     run_epilogue<C>(p, sm, ctl, tmem_base, warp - 4);
   } else {
