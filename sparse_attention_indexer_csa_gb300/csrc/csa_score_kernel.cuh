@@ -547,34 +547,61 @@ __device__ void run_scheduler(const KParams& p, const Smem<C>& sm, const WaitCtl
   }
 }
 
-// Scheduler of the document mode (C::DOCS).  The warps describe the CTA's items in order: the visible
-// tile range, per-row thresholds / segment ids / visible counts and the
-// trivial flag, and post them to two rings, each ending with an end marker
-// on the item ring:
-//  * the select warps' ring takes every item; item it is posted by warp
-//    it % 2 (its slot's parity is the item's, so every slot has one writer
-//    and is written in order);
-//  * the item ring (producer, MMA issuer, epilogue) takes, with segment ids
-//    (packed documents, where most items are trivial), only the items that
-//    need scores, all posted by warp 0 in order, so trivial items never hold
-//    a slot the tensor-core roles wait behind; without segment ids (scored
-//    and trivial items alternate) every item, posted by warp it % 2.
-// The global reads of 32 items are made at once, one item per lane, and
-// handed to the item loop through shuffles.
+// Write the selection of a row that keeps all its visible entries.
+template <int NT>
+__device__ void write_visible_set(int32_t* out, int K, int nvis, int tfirst, int contig, int thr, int seg,
+                                  const int32_t* kv, SelectScratch* sc, const Team<NT>& team) {
+  if (contig) {  // visible entries are tfirst .. tfirst + nvis - 1
+    if ((K & 3) == 0 && (reinterpret_cast<uintptr_t>(out) & 15u) == 0) {
+      int4* o4 = reinterpret_cast<int4*>(out);
+      for (int i = (int)team.tid; i < K / 4; i += NT) {
+        const int i0 = 4 * i;
+        int4 v;
+        v.x = (i0 + 0 < nvis) ? tfirst + i0 + 0 : -1;
+        v.y = (i0 + 1 < nvis) ? tfirst + i0 + 1 : -1;
+        v.z = (i0 + 2 < nvis) ? tfirst + i0 + 2 : -1;
+        v.w = (i0 + 3 < nvis) ? tfirst + i0 + 3 : -1;
+        o4[i] = v;
+      }
+    } else {
+      for (int i = (int)team.tid; i < K; i += NT) out[i] = (i < nvis) ? tfirst + i : -1;
+    }
+  } else {
+    team_write_ordered<NT>(0, thr, 0u, (uint32_t)K, out, sc, team,
+                           [&](int tt) -> int { return (kv[tt] == seg) ? 1 : 0; });
+  }
+}
+
+// Scheduler of the document mode (C::DOCS, segment summaries present).
+// The items are taken in rounds of 32: their global reads are made at once,
+// one item per lane, and handed to the item loop through shuffles; from the
+// lanes' flags both warps know, for every item of the round, where it goes.
+//  * Items that need scores go to the item ring (producer, MMA issuer,
+//    epilogue), all posted by warp 0 in order, which then ends the ring with
+//    a marker: trivial items never hold a slot the tensor-core roles wait
+//    behind.
+//  * In a round that also holds scored items, the trivial items whose rows
+//    each keep one contiguous run of visible entries -- the usual case with
+//    documents -- are written by warp 1 itself (after it has posted the
+//    round's select entries), so the select warps spend their time on the
+//    selections.
+//  * Every other item is an entry of the select warps' ring; entry e is
+//    posted by warp e % 2 (the slot's parity is the entry's, so every slot
+//    has one writer, written in order), and the ring ends with a marker.
+//    In a round of trivial items only that is every item, spread over both
+//    warps and written by the four select warps.
 template <class C>
 __device__ void run_scheduler_docs(const KParams& p, const Smem<C>& sm, const WaitCtl& ctl, int sw) {
   constexpr int R = C::R, H = C::H;
   constexpr int NWL = (R * H + 31) / 32;  // weights per lane
-  static_assert(R <= 4, "a segment summary covers four rows");
-  static_assert(!C::FUSED || C::SSLOTS % 2 == 0, "select slots alternate between the two scheduler warps");
+  static_assert(C::DOCS && R == 4, "the document mode's scheduler");
+  static_assert(C::SSLOTS % 2 == 0, "select slots alternate between the two scheduler warps");
   const uint32_t lane = lane_id();
-  const bool to_items = sw == 0;
-  const bool segs = p.q_seg != nullptr;
-  const bool pre = p.seginfo != nullptr;  // scanned ahead by csa_segscan_kernel (whole-row items)
-  const bool can_trivial = C::FUSED && p.scores == nullptr;
-  const bool only_scored = can_trivial && pre;  // item ring: the items that need scores, from warp 0
-  const int n_mine = cta_item_count<(C::R > 1)>(p);
-  int posted = 0;  // item-ring entries written so far (only_scored: warp 0)
+  const Team<32> team{0u, lane};
+  const bool can_trivial = p.scores == nullptr;  // no debug copy of the scores
+  const int n_mine = cta_item_count<true>(p);
+  int posted = 0;   // item-ring entries written (warp 0)
+  int sposted = 0;  // select-ring entries of the rounds before (both warps)
   for (int it0 = 0; it0 < n_mine; it0 += 32) {
     // lane l fetches item it0 + l
     const int my_it = it0 + (int)lane;
@@ -582,35 +609,27 @@ __device__ void run_scheduler_docs(const KParams& p, const Smem<C>& sm, const Wa
     long long qs_l = 0;
     int seg_l[R];
     SegInfo si_l{};
-    bool triv_l = false;  // known trivial (then only the select ring takes the item)
+    bool scored_l = false, ctriv_l = false;
 #pragma unroll
     for (int j = 0; j < R; ++j) seg_l[j] = 0;
     if (my_it < n_mine) {
       sched_coords<C>(p, my_it, n_mine, b_l, rb_l, c_l);
       if (p.q_start != nullptr) qs_l = p.q_start[b_l];
-      if (segs) {
 #pragma unroll
-        for (int j = 0; j < R; ++j)
-          if (rb_l * R + j < p.S) seg_l[j] = p.q_seg[(size_t)b_l * p.S + rb_l * R + j];
-      }
-      if (pre) si_l = p.seginfo[(size_t)b_l * p.n_rb + rb_l];
-      // whether the item keeps every visible entry, where a lane can tell
-      // on its own (without segment ids, or from the segment summary)
-      if (can_trivial && (!segs || pre)) {
-        int thr[R];
-        row_bounds<R>(p, qs_l, rb_l * R, thr);
-        const int c_lo = c_l * p.chunk_tiles, c_hi = min(p.n_tiles, c_lo + p.chunk_tiles);
-        bool all = true;
+      for (int j = 0; j < R; ++j)
+        if (rb_l * R + j < p.S) seg_l[j] = p.q_seg[(size_t)b_l * p.S + rb_l * R + j];
+      si_l = p.seginfo[(size_t)b_l * p.n_rb + rb_l];
+      bool triv = can_trivial, contig = true;
 #pragma unroll
-        for (int j = 0; j < R; ++j) {
-          const int nv = segs ? si_l.nvis[j] : max(0, min(thr[j], c_hi * kTileT) - c_lo * kTileT);
-          all = all && nv <= p.K;
-        }
-        triv_l = all;
+      for (int j = 0; j < R; ++j) {
+        triv = triv && si_l.nvis[j] <= p.K;
+        contig = contig && si_l.contig[j] != 0;
       }
-      if (only_scored ? to_items : ((my_it & 1) == sw)) {
-        // the weight rows of the item into L2: the item loop reads them from
-        // there if the item needs scores (a few hundred bytes per item)
+      scored_l = !triv;
+      ctriv_l = triv && contig;
+      if (sw == 0 && scored_l) {
+        // the weight rows of the item into L2: the item loop reads them
+        // from there (a few hundred bytes per item)
         const size_t esz = p.w_f32 ? 4 : 2;
 #pragma unroll
         for (int j = 0; j < R; ++j) {
@@ -623,13 +642,17 @@ __device__ void run_scheduler_docs(const KParams& p, const Smem<C>& sm, const Wa
         }
       }
     }
+    const bool mixed = __ballot_sync(0xFFFFFFFFu, scored_l) != 0u;
+    const bool w1_l = mixed && ctriv_l;  // written by warp 1
+    const uint32_t sel_mask = __ballot_sync(0xFFFFFFFFu, my_it < n_mine && !w1_l);
     const int cnt = min(32, n_mine - it0);
     for (int k = 0; k < cnt; ++k) {
-      const int it = it0 + k;
-      const bool triv_k = __shfl_sync(0xFFFFFFFFu, triv_l, k);
-      // a warp describes its own items; with only_scored, warp 0 also the
-      // other warp's items unless they are known to keep every visible entry
-      if ((it & 1) != sw && (!only_scored || !to_items || triv_k)) continue;
+      const bool w1 = __shfl_sync(0xFFFFFFFFu, w1_l, k);
+      const bool scored = __shfl_sync(0xFFFFFFFFu, scored_l, k);
+      const int e = sposted + __popc(sel_mask & ((1u << k) - 1u));  // select entry (if not w1)
+      if (w1) continue;  // written by warp 1 after the round's posts
+      const bool my_entry = (e & 1) == sw;
+      if (!my_entry && !(sw == 0 && scored)) continue;
       const int b = __shfl_sync(0xFFFFFFFFu, b_l, k);
       const int rb = __shfl_sync(0xFFFFFFFFu, rb_l, k);
       const int c = __shfl_sync(0xFFFFFFFFu, c_l, k);
@@ -637,58 +660,29 @@ __device__ void run_scheduler_docs(const KParams& p, const Smem<C>& sm, const Wa
       const int s0 = rb * R;
       int thr[R], seg[R], nvis[R], tfirst[R], contig[R];
 #pragma unroll
-      for (int j = 0; j < R; ++j) seg[j] = __shfl_sync(0xFFFFFFFFu, seg_l[j], k);
-      const int thr_max = row_bounds<R>(p, qs0, s0, thr);
+      for (int j = 0; j < R; ++j) {
+        seg[j] = __shfl_sync(0xFFFFFFFFu, seg_l[j], k);
+        nvis[j] = __shfl_sync(0xFFFFFFFFu, si_l.nvis[j], k);
+        tfirst[j] = __shfl_sync(0xFFFFFFFFu, si_l.tfirst[j], k);
+        contig[j] = __shfl_sync(0xFFFFFFFFu, si_l.contig[j], k);
+      }
+      row_bounds<R>(p, qs0, s0, thr);
       const int c_lo = c * p.chunk_tiles;
       const int c_hi = min(p.n_tiles, c_lo + p.chunk_tiles);
-      int t_lo = c_lo, t_hi = c_lo;
-      if (!segs) {
-#pragma unroll
-        for (int j = 0; j < R; ++j) {
-          nvis[j] = max(0, min(thr[j], c_hi * kTileT) - c_lo * kTileT);
-          tfirst[j] = c_lo * kTileT;
-          contig[j] = 1;
-        }
-        t_hi = max(c_lo, min(c_hi, (thr_max + kTileT - 1) / kTileT));
-      } else if (pre) {
-#pragma unroll
-        for (int j = 0; j < R; ++j) {
-          nvis[j] = __shfl_sync(0xFFFFFFFFu, si_l.nvis[j], k);
-          tfirst[j] = __shfl_sync(0xFFFFFFFFu, si_l.tfirst[j], k);
-          contig[j] = __shfl_sync(0xFFFFFFFFu, si_l.contig[j], k);
-        }
-        t_lo = __shfl_sync(0xFFFFFFFFu, si_l.t_lo, k);
-        t_hi = __shfl_sync(0xFFFFFFFFu, si_l.t_hi, k);
-      } else {
-        scan_segments<R>(p, b, c_lo * kTileT, min(c_hi * kTileT, thr_max), thr, seg, nvis, tfirst, contig, t_lo,
-                         t_hi);
+      const int t_lo = __shfl_sync(0xFFFFFFFFu, si_l.t_lo, k);
+      const int t_hi = scored ? __shfl_sync(0xFFFFFFFFu, si_l.t_hi, k) : t_lo;
+      const int trivial = scored ? 0 : 1;
+      if (my_entry) {  // the select ring
+        const int ss = e % C::SSLOTS;
+        mbar_wait(sm.sel_empty(ss), ((e / C::SSLOTS) & 1) ^ 1, ctl);
+        if (lane == 0)
+          write_desc<R>(sm.sdesc(ss), b, s0, t_lo, t_hi, c_lo, c_hi, trivial, thr, seg, nvis, tfirst, contig);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(sm.sel_full(ss));
       }
-      int trivial = 0;
-      if (can_trivial) {
-        trivial = 1;
-#pragma unroll
-        for (int j = 0; j < R; ++j) trivial &= (nvis[j] <= p.K) ? 1 : 0;
-        if (trivial) t_hi = t_lo;
-      }
-      if constexpr (C::FUSED) {
-        if ((it & 1) == sw) {  // the select ring
-          const int ss = it % C::SSLOTS;
-          mbar_wait(sm.sel_empty(ss), ((it / C::SSLOTS) & 1) ^ 1, ctl);
-          if (lane == 0)
-            write_desc<R>(sm.sdesc(ss), b, s0, t_lo, t_hi, c_lo, c_hi, trivial, thr, seg, nvis, tfirst, contig);
-          __syncwarp();
-          if (lane == 0) mbar_arrive(sm.sel_full(ss));
-        }
-      }
-      int ki;  // item-ring entry
-      if (only_scored) {
-        if (!to_items || trivial) continue;  // the select warps alone handle a trivial item
-        ki = posted++;
-      } else {
-        ki = it;  // this warp's own item, trivial or not
-      }
-      // the weights (fp32) of a scored item's rows, every load in flight
-      // before the first store; rows past S get 0
+      if (sw != 0 || !scored) continue;
+      // the item ring, with the weights (fp32) of the item's rows: every
+      // load in flight before the first store; rows past S get 0
       float wv[NWL];
 #pragma unroll
       for (int u = 0; u < NWL; ++u) {
@@ -696,34 +690,57 @@ __device__ void run_scheduler_docs(const KParams& p, const Smem<C>& sm, const Wa
         const int j = i / H, h = i % H;
         const int s = s0 + j;
         float v = 0.f;
-        if (!trivial && i < R * H && s < p.S) {
+        if (i < R * H && s < p.S) {
           const size_t off = (size_t)b * p.w_sb + (size_t)s * p.w_ss + h;
           v = p.w_f32 ? reinterpret_cast<const float*>(p.w)[off]
                       : __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p.w)[off]);
         }
         wv[u] = v;
       }
-      const int slot = ki % C::SLOTS;
-      mbar_wait(sm.item_empty(slot), ((ki / C::SLOTS) & 1) ^ 1, ctl);
-      if (!trivial) {
-        float* ws = sm.w(slot);
+      const int slot = posted % C::SLOTS;
+      mbar_wait(sm.item_empty(slot), ((posted / C::SLOTS) & 1) ^ 1, ctl);
+      float* ws = sm.w(slot);
 #pragma unroll
-        for (int u = 0; u < NWL; ++u) {
-          const int i = (int)lane + 32 * u;
-          if (i < R * H) ws[i] = wv[u];
-        }
+      for (int u = 0; u < NWL; ++u) {
+        const int i = (int)lane + 32 * u;
+        if (i < R * H) ws[i] = wv[u];
       }
       if (lane == 0) write_desc<R>(sm.desc(slot), b, s0, t_lo, t_hi, c_lo, c_hi, trivial, thr, seg, nvis, tfirst, contig);
       __syncwarp();
       if (lane == 0) mbar_arrive(sm.item_full(slot));
+      ++posted;
     }
+    if (sw == 1 && mixed) {
+      // the round's contiguous trivial items: each row's visible entries
+      // tfirst .. tfirst + nvis - 1, -1 padded
+      for (int k = 0; k < cnt; ++k) {
+        if (!__shfl_sync(0xFFFFFFFFu, w1_l, k)) continue;
+        const int b = __shfl_sync(0xFFFFFFFFu, b_l, k);
+        const int rb = __shfl_sync(0xFFFFFFFFu, rb_l, k);
+#pragma unroll
+        for (int j = 0; j < R; ++j) {
+          const int nv = __shfl_sync(0xFFFFFFFFu, si_l.nvis[j], k);
+          const int tf = __shfl_sync(0xFFFFFFFFu, si_l.tfirst[j], k);
+          const int s = rb * R + j;
+          if (s < p.S)
+            write_visible_set<32>(p.idx + ((size_t)b * p.S + s) * p.K, p.K, nv, tf, 1, 0, 0, nullptr, nullptr, team);
+        }
+      }
+    }
+    sposted += __popc(sel_mask);
   }
-  // end marker (b < 0) after the last item-ring entry: from warp 0 with
-  // only_scored, else from the warp whose parity the entry index has
-  const int end_at = only_scored ? posted : n_mine;
-  if (only_scored ? to_items : ((end_at & 1) == sw)) {
-    const int slot = end_at % C::SLOTS;
-    mbar_wait(sm.item_empty(slot), ((end_at / C::SLOTS) & 1) ^ 1, ctl);
+  // the end markers (b < 0): the select ring's from the warp of its
+  // entry's parity, the item ring's from warp 0
+  if ((sposted & 1) == sw) {
+    const int ss = sposted % C::SSLOTS;
+    mbar_wait(sm.sel_empty(ss), ((sposted / C::SSLOTS) & 1) ^ 1, ctl);
+    if (lane == 0) sm.sdesc(ss)->b = -1;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(sm.sel_full(ss));
+  }
+  if (sw == 0) {
+    const int slot = posted % C::SLOTS;
+    mbar_wait(sm.item_empty(slot), ((posted / C::SLOTS) & 1) ^ 1, ctl);
     if (lane == 0) sm.desc(slot)->b = -1;
     __syncwarp();
     if (lane == 0) mbar_arrive(sm.item_full(slot));
@@ -918,31 +935,6 @@ __device__ __forceinline__ void epilogue_accumulate(uint32_t t_row, const float*
   }
 }
 
-// Write the selection of a row that keeps all its visible entries.
-template <int NT>
-__device__ void write_visible_set(int32_t* out, int K, int nvis, int tfirst, int contig, int thr, int seg,
-                                  const int32_t* kv, SelectScratch* sc, const Team<NT>& team) {
-  if (contig) {  // visible entries are tfirst .. tfirst + nvis - 1
-    if ((K & 3) == 0 && (reinterpret_cast<uintptr_t>(out) & 15u) == 0) {
-      int4* o4 = reinterpret_cast<int4*>(out);
-      for (int i = (int)team.tid; i < K / 4; i += NT) {
-        const int i0 = 4 * i;
-        int4 v;
-        v.x = (i0 + 0 < nvis) ? tfirst + i0 + 0 : -1;
-        v.y = (i0 + 1 < nvis) ? tfirst + i0 + 1 : -1;
-        v.z = (i0 + 2 < nvis) ? tfirst + i0 + 2 : -1;
-        v.w = (i0 + 3 < nvis) ? tfirst + i0 + 3 : -1;
-        o4[i] = v;
-      }
-    } else {
-      for (int i = (int)team.tid; i < K; i += NT) out[i] = (i < nvis) ? tfirst + i : -1;
-    }
-  } else {
-    team_write_ordered<NT>(0, thr, 0u, (uint32_t)K, out, sc, team,
-                           [&](int tt) -> int { return (kv[tt] == seg) ? 1 : 0; });
-  }
-}
-
 template <class C>
 __device__ void run_epilogue(const KParams& p, const Smem<C>& sm, const WaitCtl& ctl, uint32_t tmem_base,
                              int e /* epilogue warp 0..EW-1 */) {
@@ -1068,16 +1060,18 @@ __device__ void run_selector(const KParams& p, const Smem<C>& sm, const WaitCtl&
   const Team<32> team{0u, lane};
   FusedRowScratch* fs = sm.scratch(j);
   uint32_t nt = 0;
-  const int n_mine = cta_item_count<(C::R > 1)>(p);
+  // document mode: the select ring until its end marker
+  const int n_mine = C::DOCS ? 0x7FFFFFFF : cta_item_count<(C::R > 1)>(p);
   for (int it = 0; it < n_mine; ++it) {
     const int ss = it % C::SSLOTS;
-    mbar_wait(sm.sel_full(ss), (it / C::SSLOTS) & 1, ctl);
+    const bool ok_s = mbar_wait(sm.sel_full(ss), (it / C::SSLOTS) & 1, ctl);
     const ItemDesc<R>* d = sm.sdesc(ss);
     const int b = d->b, s0 = d->s0, s = s0 + j;
     const int trivial = d->trivial, t_lo = d->t_lo, t_hi = d->t_hi;
     const int nvis = d->nvis[j], tfirst = d->tfirst[j], contig = d->contig[j], thr = d->thr[j], seg = d->seg[j];
     __syncwarp();
     if (lane == 0) mbar_arrive(sm.sel_empty(ss));
+    if (C::DOCS && (!ok_s || b < 0)) break;
     int32_t* out = p.idx + ((size_t)b * p.S + s) * p.K;
     if (trivial) {
       if (s < p.S)
