@@ -35,6 +35,25 @@ cudaError_t smem_limit_once(int bytes) {
   return e;
 }
 
+// Launch of `kernel` on `stream` with programmatic stream serialization: it
+// may start while the previous kernel on the stream finishes, and waits in
+// griddep_wait() before reading global memory.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // Which instantiation of the persistent kernel to launch.
 struct KernelChoice {
   int H, D, R;

@@ -161,6 +161,19 @@ __device__ __forceinline__ void umma_commit_u32(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
 }
 
+// ----------------------------------------------------------------- dependent launches
+// A kernel launched with programmatic stream serialization may start before
+// the previous kernel on its stream has finished: it waits here, before
+// reading any global memory, until that kernel's results are visible.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Lets the next kernel on the stream launch (its CTAs then wait in
+// griddep_wait); only for single-wave kernels, whose CTAs are all resident
+// (a multi-wave kernel's later CTAs could find the SMs held by waiting
+// dependents).
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ----------------------------------------------------------------- TMA
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(m) : "memory");

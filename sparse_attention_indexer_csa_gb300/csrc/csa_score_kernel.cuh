@@ -1236,6 +1236,14 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
   tc_fence_after();
   const uint32_t tmem_base = *sm.tmem_slot();
   const WaitCtl ctl{sm.abort_flag(), p.wait_ns};
+  // launched as a dependent (document mode, after the segment pre-pass): the
+  // previous kernel's results (our inputs) are visible past this point;
+  // every CTA of this single-wave grid is resident, so the next kernel may
+  // start its own set-up on the SMs this one leaves
+  if constexpr (C::DOCS) {
+    griddep_wait();
+    griddep_launch_dependents();
+  }
 
   if (warp == 0) {
     if (lane == 0) run_producer<C>(p, sm, ctl, &tmap_q, &tmap_k);
