@@ -16,7 +16,8 @@
  *
  * Conventions shared by every entry point
  * ---------------------------------------
- *  - All tensor pointers are DEVICE pointers owned by the caller, row-major
+ *  - All tensor pointers are DEVICE pointers owned by the caller (except
+ *    those of csa_index_fused_host, which are host pointers), row-major
  *    (contiguous unless csa_problem gives strides for q, k or w), with
  *    16-byte aligned bases.  The library never allocates,
  *    frees or synchronises in these calls; work is enqueued on `stream`
@@ -141,6 +142,41 @@ csa_status csa_index_fused(const csa_problem* p, const void* q, const void* k, c
                            int32_t* idx, float* scores_dbg, void* workspace,
                            size_t workspace_bytes, void* stream);
 
+/* csa_index_fused on HOST buffers (added in ABI version 106): q, k, w,
+ * q_seg, kv_seg, q_start and idx are host pointers (page-locked memory
+ * makes the copies asynchronous), contiguous and in the layouts of
+ * csa_index_fused (each stride in csa_problem 0 or the contiguous one).  The call
+ * enqueues on `stream`, in order: the copies of the inputs into
+ * `workspace`, the computation of csa_index_fused, and the copy of idx
+ * back to the host; it returns without waiting, so idx may be read, and the
+ * input buffers reused, only after the stream has been synchronised.
+ * q_start, when given, is also read on the host during the call.
+ * Only the q rows the computation can read are copied.  A row whose
+ * future-mask bound min(W, (pos + 1) / compress_rate) is at most top_k
+ * keeps all its visible entries, whatever its scores; when csa_index_fused
+ * runs as one kernel, the q block of an item of four such rows is never
+ * loaded, so the rows before the first item holding a row with a larger
+ * bound are not transferred (on prefill with q_start = 0 that is rows
+ * s < ((top_k + 1) * compress_rate - 1) rounded down to a multiple of 4).
+ * The other paths copy all of q.  csa_index_fused_host_bytes() gives the
+ * bytes one call moves each way.
+ * Needs `workspace`: csa_index_workspace_size(p, 3) bytes of device memory
+ * owned by the caller, 256-byte aligned, holding the device copies of the
+ * inputs and of idx and csa_index_fused's own workspace; calls that may be
+ * in flight at the same time need separate workspaces.  Errors: as for
+ * csa_index_fused; a stride other than the contiguous one returns
+ * CSA_ERR_INVALID_ARG.                                                    */
+csa_status csa_index_fused_host(const csa_problem* p, const void* q, const void* k, const void* w,
+                                const int32_t* q_seg, const int32_t* kv_seg, const int64_t* q_start,
+                                int32_t* idx, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Bytes one csa_index_fused_host call copies host -> device (*h2d: the q
+ * rows it transfers, k, w, the segment ids when with_segments != 0, and
+ * q_start when given) and device -> host (*d2h: idx).  q_start is the host
+ * array the call would get (NULL = 0).  Enqueues nothing.                 */
+csa_status csa_index_fused_host_bytes(const csa_problem* p, const int64_t* q_start, int32_t with_segments,
+                                      size_t* h2d, size_t* d2h);
+
 /* Gather of the selected compressed entries, the rows sparse attention reads
  * ("DSV4: Add indexer_save_selection and indexer_sharded_topk", Description:
  * the selection is handed to sparse attention in sequence layout):
@@ -212,8 +248,8 @@ csa_status csa_index_backward(const csa_problem* p, const void* q, const void* k
 
 /* Bytes of device workspace an entry point needs: which = 0 for
  * csa_index_topk (always 0), 1 for csa_index_fused, 2 for
- * csa_index_backward.  Depends only on the problem (no device query).
- * Returns 0 when the problem is invalid.                                  */
+ * csa_index_backward, 3 for csa_index_fused_host.  Depends only on the
+ * problem (no device query).  Returns 0 when the problem is invalid.      */
 size_t csa_index_workspace_size(const csa_problem* p, int32_t which);
 
 /* Synchronises `stream`, then reads and clears the device status word of
@@ -229,8 +265,9 @@ csa_status csa_index_selftest_timeout(uint32_t timeout_us, void* stream);
 /* Static string for a status code. */
 const char* csa_status_string(csa_status s);
 
-/* ABI version (major * 100 + minor): 105 (backward workspace holds the
- * segment summaries; 104: strides in csa_problem). */
+/* ABI version (major * 100 + minor): 106 (csa_index_fused_host; 105:
+ * backward workspace holds the segment summaries; 104: strides in
+ * csa_problem). */
 int32_t csa_index_abi_version(void);
 
 #ifdef __cplusplus

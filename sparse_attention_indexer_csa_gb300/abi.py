@@ -25,6 +25,8 @@ EXPORTED = (
     "csa_index_topk",
     "csa_index_fused",
     "csa_index_fused_noalloc",
+    "csa_index_fused_host",
+    "csa_index_fused_host_bytes",
     "csa_index_gather",
     "csa_index_backward",
     "csa_index_workspace_size",
@@ -73,6 +75,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.csa_index_topk.argtypes = [P, vp, vp, vp, sz, vp]
     lib.csa_index_fused.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     lib.csa_index_fused_noalloc.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp]
+    lib.csa_index_fused_host.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.csa_index_fused_host_bytes.argtypes = [P, vp, i32, ctypes.POINTER(sz), ctypes.POINTER(sz)]
     lib.csa_index_gather.argtypes = [P, vp, vp, vp, vp]
     lib.csa_index_backward.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     lib.csa_index_workspace_size.argtypes = [P, i32]
@@ -82,7 +86,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.csa_status_string.argtypes = [i32]
     lib.csa_status_string.restype = ctypes.c_char_p
     lib.csa_index_abi_version.restype = i32
-    for name in ("csa_index_score", "csa_index_topk", "csa_index_fused", "csa_index_fused_noalloc", "csa_index_gather",
+    for name in ("csa_index_score", "csa_index_topk", "csa_index_fused", "csa_index_fused_noalloc",
+                 "csa_index_fused_host", "csa_index_fused_host_bytes", "csa_index_gather",
                  "csa_index_backward",
                  "csa_index_device_status",
                  "csa_index_selftest_timeout"):
@@ -175,6 +180,34 @@ def index_fused_noalloc_raw(p: Problem, q, k, w, q_seg, kv_seg, q_start, idx, st
                                           _ptr(q_start), _ptr(idx), _stream(stream))
 
 
+def _host_ptr(t: Optional[torch.Tensor]):
+    """Host pointer of a contiguous CPU tensor (csa_index_fused_host)."""
+    if t is None:
+        return None
+    if t.is_cuda:
+        raise ValueError("csa_index_fused_host takes host (CPU) tensors")
+    if not t.is_contiguous():
+        raise ValueError("host tensors passed to the library must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def index_fused_host_raw(p: Problem, q, k, w, q_seg, kv_seg, q_start, idx, workspace, stream=None) -> int:
+    """csa_index_fused_host: host inputs and idx, device `workspace`."""
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    return load().csa_index_fused_host(ctypes.byref(p), _host_ptr(q), _host_ptr(k), _host_ptr(w), _host_ptr(q_seg),
+                                       _host_ptr(kv_seg), _host_ptr(q_start), _host_ptr(idx), _ptr(workspace),
+                                       nbytes, _stream(stream))
+
+
+def fused_host_bytes(p: Problem, q_start=None, with_segments: bool = False):
+    """(host->device, device->host) bytes of one csa_index_fused_host call."""
+    h2d, d2h = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    _check("csa_index_fused_host_bytes",
+           load().csa_index_fused_host_bytes(ctypes.byref(p), _host_ptr(q_start), 1 if with_segments else 0,
+                                             ctypes.byref(h2d), ctypes.byref(d2h)))
+    return int(h2d.value), int(d2h.value)
+
+
 def index_backward_raw(p: Problem, q, k, w, q_seg, kv_seg, q_start, g, dq, dk, dw, workspace=None,
                        stream=None) -> int:
     nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
@@ -228,6 +261,21 @@ def index_fused(q, k, w, scale, compress_rate, top_k, q_seg=None, kv_seg=None, q
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     _check("csa_index_fused", index_fused_raw(p, q, k, w, q_seg, kv_seg, q_start, out, scores_dbg,
                                               workspace, stream))
+    return out
+
+
+def index_fused_host(q, k, w, scale, compress_rate, top_k, q_seg=None, kv_seg=None, q_start=None, out=None,
+                     workspace=None, stream=None, q_layout=CSA_Q_HEAD_MAJOR, device=None):
+    """csa_index_fused on host tensors (pinned for asynchronous copies) ->
+    idx [B,S,top_k] int32 on the host, valid once `stream` has been
+    synchronised (this helper does not wait)."""
+    p = make_problem(q, k, w, scale, compress_rate, top_k, q_layout)
+    if out is None:
+        out = torch.empty(p.B, p.S, p.top_k, dtype=torch.int32, pin_memory=True)
+    if workspace is None:
+        workspace = torch.empty(workspace_size(p, 3), dtype=torch.uint8,
+                                device=device if device is not None else torch.cuda.current_device())
+    _check("csa_index_fused_host", index_fused_host_raw(p, q, k, w, q_seg, kv_seg, q_start, out, workspace, stream))
     return out
 
 

@@ -248,6 +248,80 @@ size_t fused_workspace_bytes(const csa_problem* p) {
   return (size_t)p->B * p->S * p->W * sizeof(float);
 }
 
+// ----------------------------------------------------------------- host buffers
+// Device workspace of csa_index_fused_host: the inputs' device copies, idx
+// and csa_index_fused's own workspace, each 256-byte aligned.
+struct HostPlan {
+  size_t q, k, w, qseg, kvseg, qst, idx, fws;              // bytes
+  size_t off_q, off_k, off_w, off_qseg, off_kvseg, off_qst, off_idx, off_fws, total;
+};
+size_t up256(size_t x) { return (x + 255) & ~(size_t)255; }
+HostPlan host_plan(const csa_problem* p) {
+  HostPlan h{};
+  const size_t B = (size_t)p->B, S = (size_t)p->S, W = (size_t)p->W;
+  h.q = B * (size_t)p->H * S * (size_t)p->D * 2;
+  h.k = B * W * (size_t)p->D * 2;
+  h.w = B * S * (size_t)p->H * (p->w_dtype == CSA_F32 ? 4 : 2);
+  h.qseg = B * S * 4;
+  h.kvseg = B * W * 4;
+  h.qst = B * 8;
+  h.idx = B * S * (size_t)p->top_k * 4;
+  h.fws = fused_workspace_bytes(p);
+  size_t o = 0;
+  h.off_q = o;
+  o = up256(o + h.q);
+  h.off_k = o;
+  o = up256(o + h.k);
+  h.off_w = o;
+  o = up256(o + h.w);
+  h.off_qseg = o;
+  o = up256(o + h.qseg);
+  h.off_kvseg = o;
+  o = up256(o + h.kvseg);
+  h.off_qst = o;
+  o = up256(o + h.qst);
+  h.off_idx = o;
+  o = up256(o + h.idx);
+  h.off_fws = o;
+  h.total = up256(o + h.fws);
+  return h;
+}
+
+// First query row of a sequence starting at position qs whose q the
+// one-kernel fused path can read.  An item of four rows is scored only if
+// one of its rows sees more than top_k entries, which needs that row's
+// future-mask bound min(W, (qs + s + 1) / r) to exceed top_k, i.e. W > top_k
+// and qs + s + 1 >= (top_k + 1) * r.  Bounds grow with s, so every item
+// before the one holding the first such row keeps its visible sets without
+// its q block ever being loaded.  The other paths read all of q.
+int first_read_row(const csa_problem* p, long long qs) {
+  if (!fused_one_kernel(p)) return 0;
+  if (p->W <= p->top_k) return p->S;
+  const long long lim = 1ll << 62;
+  qs = qs < -lim ? -lim : (qs > lim ? lim : qs);
+  const long long s = (long long)(p->top_k + 1) * p->compress_rate - qs - 1;
+  if (s >= p->S) return p->S;
+  return s <= 0 ? 0 : (int)(s / 4 * 4);
+}
+
+// Host -> device bytes of q that csa_index_fused_host copies.
+size_t host_q_bytes(const csa_problem* p, const int64_t* q_start) {
+  size_t n = 0;
+  for (int b = 0; b < p->B; ++b)
+    n += (size_t)(p->S - first_read_row(p, q_start ? q_start[b] : 0)) * (size_t)p->H * (size_t)p->D * 2;
+  return n;
+}
+
+// Host buffers are contiguous: every stride is 0 or the contiguous one.
+bool host_layout_ok(const csa_problem* p) {
+  csa_problem dense = *p;
+  dense.q_stride_b = dense.q_stride_h = dense.q_stride_s = 0;
+  dense.k_stride_b = dense.k_stride_w = dense.w_stride_b = dense.w_stride_s = 0;
+  const Strides a = strides_of(p), c = strides_of(&dense);
+  return a.qb == c.qb && a.qh == c.qh && a.qs == c.qs && a.kb == c.kb && a.kw == c.kw && a.wb == c.wb &&
+         a.ws == c.ws;
+}
+
 // ----------------------------------------------------------------- allocation-free variant
 // Scratch for csa_index_fused_noalloc: the fp32 scores of one call, at most
 // kNoAllocMaxScores of them (8 MiB).  Every GPU that loads the library keeps
@@ -344,6 +418,64 @@ csa_status csa_index_fused(const csa_problem* p, const void* q, const void* k, c
   return CSA_OK;
 }
 
+csa_status csa_index_fused_host(const csa_problem* p, const void* q, const void* k, const void* w,
+                                const int32_t* q_seg, const int32_t* kv_seg, const int64_t* q_start, int32_t* idx,
+                                void* workspace, size_t workspace_bytes, void* stream) {
+  csa_status st = check_problem(p);
+  if (st != CSA_OK) return st;
+  if (q == nullptr || k == nullptr || w == nullptr || idx == nullptr) return CSA_ERR_INVALID_ARG;
+  if ((q_seg == nullptr) != (kv_seg == nullptr)) return CSA_ERR_INVALID_ARG;
+  if (!host_layout_ok(p)) return CSA_ERR_INVALID_ARG;
+  if (!shape_supported(p)) return CSA_ERR_UNSUPPORTED;
+  if (!fused_one_kernel(p) && p->W > kTopkMaxW) return CSA_ERR_UNSUPPORTED;
+  const HostPlan h = host_plan(p);
+  if (workspace == nullptr || workspace_bytes < h.total || !aligned(workspace, 256)) return CSA_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  auto in = [&](size_t off, const void* src, size_t n) {
+    return n == 0 || cudaMemcpyAsync(ws + off, src, n, cudaMemcpyHostToDevice, s) == cudaSuccess;
+  };
+  // q: only the rows the computation can read (whole items of four rows)
+  const size_t row = (size_t)p->D * 2;
+  for (int b = 0; b < p->B; ++b) {
+    const int s0 = first_read_row(p, q_start ? q_start[b] : 0);
+    if (s0 >= p->S) continue;
+    const size_t rows = (size_t)(p->S - s0);
+    const uint8_t* hq = static_cast<const uint8_t*>(q);
+    if (p->q_layout == CSA_Q_HEAD_MAJOR) {  // H slabs of S rows: one strided copy
+      const size_t pitch = (size_t)p->S * row, off = ((size_t)b * p->H * p->S + (size_t)s0) * row;
+      if (cudaMemcpy2DAsync(ws + h.off_q + off, pitch, hq + off, pitch, rows * row, (size_t)p->H,
+                            cudaMemcpyHostToDevice, s) != cudaSuccess)
+        return CSA_ERR_CUDA;
+    } else {  // rows of H heads: one contiguous range
+      const size_t off = ((size_t)b * p->S + (size_t)s0) * (size_t)p->H * row;
+      if (!in(h.off_q + off, hq + off, rows * (size_t)p->H * row)) return CSA_ERR_CUDA;
+    }
+  }
+  if (!in(h.off_k, k, h.k) || !in(h.off_w, w, h.w)) return CSA_ERR_CUDA;
+  if (q_seg != nullptr && (!in(h.off_qseg, q_seg, h.qseg) || !in(h.off_kvseg, kv_seg, h.kvseg))) return CSA_ERR_CUDA;
+  if (q_start != nullptr && !in(h.off_qst, q_start, h.qst)) return CSA_ERR_CUDA;
+  st = csa_index_fused(p, ws + h.off_q, ws + h.off_k, ws + h.off_w,
+                       q_seg ? reinterpret_cast<const int32_t*>(ws + h.off_qseg) : nullptr,
+                       kv_seg ? reinterpret_cast<const int32_t*>(ws + h.off_kvseg) : nullptr,
+                       q_start ? reinterpret_cast<const int64_t*>(ws + h.off_qst) : nullptr,
+                       reinterpret_cast<int32_t*>(ws + h.off_idx), nullptr, ws + h.off_fws, h.fws, stream);
+  if (st != CSA_OK) return st;
+  if (cudaMemcpyAsync(idx, ws + h.off_idx, h.idx, cudaMemcpyDeviceToHost, s) != cudaSuccess) return CSA_ERR_CUDA;
+  return CSA_OK;
+}
+
+csa_status csa_index_fused_host_bytes(const csa_problem* p, const int64_t* q_start, int32_t with_segments,
+                                      size_t* h2d, size_t* d2h) {
+  csa_status st = check_problem(p);
+  if (st != CSA_OK) return st;
+  if (h2d == nullptr || d2h == nullptr) return CSA_ERR_INVALID_ARG;
+  const HostPlan h = host_plan(p);
+  *h2d = host_q_bytes(p, q_start) + h.k + h.w + (with_segments ? h.qseg + h.kvseg : 0) + (q_start ? h.qst : 0);
+  *d2h = h.idx;
+  return CSA_OK;
+}
+
 csa_status csa_index_fused_noalloc(const csa_problem* p, const void* q, const void* k, const void* w,
                                    const int32_t* q_seg, const int32_t* kv_seg, const int64_t* q_start,
                                    int32_t* idx, void* stream) {
@@ -370,6 +502,7 @@ csa_status csa_index_fused_noalloc(const csa_problem* p, const void* q, const vo
 size_t csa_index_workspace_size(const csa_problem* p, int32_t which) {
   if (which == 1) return fused_workspace_bytes(p);
   if (which == 2) return backward_workspace_bytes(p);
+  if (which == 3) return check_problem(p) == CSA_OK ? host_plan(p).total : 0;
   return 0;
 }
 
@@ -496,6 +629,6 @@ const char* csa_status_string(csa_status s) {
   return "unknown status";
 }
 
-int32_t csa_index_abi_version(void) { return 105; }
+int32_t csa_index_abi_version(void) { return 106; }
 
 }  // extern "C"

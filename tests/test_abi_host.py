@@ -39,7 +39,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_abi_version_and_strings(lib):
-    assert lib.csa_index_abi_version() == 105
+    assert lib.csa_index_abi_version() == 106
     for s in range(6):
         assert abi.status_string(s)
     assert abi.status_string(99) == "unknown status"
@@ -159,3 +159,87 @@ def test_backward_argument_checks(lib):
     assert _bwd(lib, _p(), dk=ctypes.c_void_p(0x10008)) == abi.CSA_ERR_INVALID_ARG
     # only H=64, D=128
     assert _bwd(lib, _p(H=4, D=32)) == abi.CSA_ERR_UNSUPPORTED
+
+
+# ----------------------------------------------------------------------------- host-buffer entry point
+def _up(x):
+    return (x + 255) // 256 * 256
+
+
+def _host_ws(p):
+    """csa_index_workspace_size(p, 3) restated: q, k, w, both id arrays,
+    q_start, idx and csa_index_fused's workspace, each 256-byte aligned."""
+    wsz = 2 if p.w_dtype == abi.CSA_BF16 else 4
+    parts = [p.B * p.H * p.S * p.D * 2, p.B * p.W * p.D * 2, p.B * p.S * p.H * wsz, p.B * p.S * 4, p.B * p.W * 4,
+             p.B * 8, p.B * p.S * p.top_k * 4, abi.workspace_size(p, 1)]
+    return sum(_up(x) for x in parts)
+
+
+@pytest.mark.parametrize("kw", [dict(), dict(B=2, S=16384, W=4096, top_k=2048), dict(W=9000, S=300),
+                                dict(S=1, W=32768, top_k=2048), dict(w_dtype=abi.CSA_F32, q_layout=1)])
+def test_host_workspace_size(lib, kw):
+    p = _p(**kw)
+    assert abi.workspace_size(p, 3) == _host_ws(p)
+
+
+def _host_bytes(p, q_start=None, segs=False):
+    import torch
+    st = None if q_start is None else torch.tensor(q_start, dtype=torch.int64)
+    return abi.fused_host_bytes(p, st, segs)
+
+
+def test_host_bytes_prefill_16k(lib):
+    """prefill B=2 S=16384 W=4096 top_k=2048: rows s < 8195 see at most 2048
+    entries; the item of rows 8192..8195 is the first that can be scored, so
+    rows 8192.. of each batch are sent (half of q)."""
+    p = _p(B=2, S=16384, W=4096, top_k=2048)
+    h2d, d2h = _host_bytes(p)
+    q_rows = 2 * (16384 - 8192) * 64 * 128 * 2
+    assert h2d == q_rows + 2 * 4096 * 128 * 2 + 2 * 16384 * 64 * 2
+    assert d2h == 2 * 16384 * 2048 * 4
+    # sequence-major q: the same rows
+    assert _host_bytes(_p(B=2, S=16384, W=4096, top_k=2048, q_layout=1)) == (h2d, d2h)
+
+
+def test_host_bytes_follow_offsets_ids_and_paths(lib):
+    row = 64 * 128 * 2
+    base = 2 * 4096 * 128 * 2 + 2 * 16384 * 64 * 2
+    p = _p(B=2, S=16384, W=4096, top_k=2048)
+    # a sequence starting at position 8000 sees more than top_k entries from
+    # row 196 ((2048 + 1) * 4 - 8000 - 1 = 195 -> item of rows 192..195);
+    # one starting at 100000 from its first row
+    h2d, _ = _host_bytes(p, q_start=[8000, 100000])
+    assert h2d == (16384 - 192) * row + 16384 * row + base + 2 * 8
+    # segment ids are sent when given
+    h2d_s, _ = _host_bytes(p, segs=True)
+    assert h2d_s == 2 * 8192 * row + base + 2 * 16384 * 4 + 2 * 4096 * 4
+    # W <= top_k: every row keeps its visible set, no q row is sent
+    p = _p(B=1, S=4096, W=1024, top_k=1024)
+    assert _host_bytes(p)[0] == 1024 * 128 * 2 + 4096 * 64 * 2
+    # single-row problems and rows past 16384 entries take two passes: all of q
+    for kw in (dict(B=3, S=1, W=32768, top_k=2048), dict(B=1, S=64, W=20000, top_k=2048)):
+        p = _p(**kw)
+        h2d, _ = _host_bytes(p)
+        assert h2d == p.B * p.S * row + p.B * p.W * 128 * 2 + p.B * p.S * 64 * 2
+
+
+def _host_call(lib, p, q=FAKE, k=FAKE, w=FAKE, qs=None, kvs=None, st=None, out=FAKE, ws=FAKE, nbytes=None):
+    nbytes = abi.workspace_size(p, 3) if nbytes is None else nbytes
+    return lib.csa_index_fused_host(ctypes.byref(p), q, k, w, qs, kvs, st, out, ws, nbytes, None)
+
+
+def test_host_entry_argument_checks(lib):
+    """Every check returns before a copy is enqueued (no GPU here)."""
+    p = _p(S=64, W=16, top_k=4)
+    assert _host_call(lib, p, q=None) == abi.CSA_ERR_INVALID_ARG
+    assert _host_call(lib, p, out=None) == abi.CSA_ERR_INVALID_ARG
+    assert _host_call(lib, p, qs=FAKE) == abi.CSA_ERR_INVALID_ARG  # ids of one side only
+    assert _host_call(lib, p, ws=None) == abi.CSA_ERR_INVALID_ARG
+    assert _host_call(lib, p, ws=ctypes.c_void_p(0x10010)) == abi.CSA_ERR_INVALID_ARG  # not 256-byte aligned
+    assert _host_call(lib, p, nbytes=abi.workspace_size(p, 3) - 1) == abi.CSA_ERR_INVALID_ARG
+    strided = _p(S=64, W=16, top_k=4, q_stride_s=256)  # rows further apart than D
+    assert _host_call(lib, strided) == abi.CSA_ERR_INVALID_ARG
+    dense = _p(S=64, W=16, top_k=4, q_stride_b=64 * 64 * 128, q_stride_h=64 * 128, q_stride_s=128)
+    assert _host_call(lib, dense, ws=None) == abi.CSA_ERR_INVALID_ARG  # the strides pass; the workspace does not
+    assert _host_call(lib, _p(S=64, W=16, top_k=4, H=8)) == abi.CSA_ERR_UNSUPPORTED
+    assert _host_call(lib, _p(S=1, W=60000, top_k=4)) == abi.CSA_ERR_UNSUPPORTED
