@@ -234,9 +234,6 @@ __device__ __forceinline__ int cta_item(int k) {
   return ROT ? k * g + ((int)blockIdx.x + k) % g : k * g + (int)blockIdx.x;
 }
 
-// Rows s0 .. s0+R-1 of batch b: each row's visible bound min(W, (pos+1)/r)
-// under the future mask (0 for rows past S) and its segment id (0 without
-// segments); returns the largest bound.
 // Visible bound min(W, (pos+1)/r) of rows s0 .. s0+R-1 of a sequence that
 // starts at position qs0 (0 for rows past S); returns the largest.
 template <int R>
