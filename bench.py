@@ -553,6 +553,11 @@ def run_ours(args, wl, inp):
                 line[key] = side_leg(side, dev, stream)
             except Exception as ex:  # reported, never hides the headline line
                 line[key] = {"error": str(ex)[:300]}
+        if args.packed_seeds > 0:
+            try:
+                line["packed_seeds"] = packed_seeds_leg(args.packed_seeds, dev, stream)
+            except Exception as ex:
+                line["packed_seeds"] = {"error": str(ex)[:300]}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cb = oracle_sample(inp, args.cpu_seconds)
         line["cpu_baseline"] = {"value": cb["tflops"], "unit": "TFLOP/s", "cores": os.cpu_count(),
@@ -624,6 +629,26 @@ def side_leg(wl, dev, stream, steps=50, warmup=5):
                            "achieved_counts": "2*H*D per visible pair of rows with visible > top_k"}
     del q, k, w, qs, ks, st, idx, ws
     return out
+
+
+def packed_seeds_leg(n, dev, stream):
+    """The packed-document workload over generator seeds 0 .. n-1 (documents
+    and so the work differ by seed): each seed timed on its own, then the
+    average over the seeds -- total useful work over total time."""
+    per = []
+    for seed in range(n):
+        r = side_leg(WORKLOADS["packed_8k"].with_(seed=seed), dev, stream, steps=20, warmup=3)
+        per.append(r)
+    t = sum(r["ms_per_step"] for r in per)
+    fl = sum(r["tflops_nontrivial_rows"] * r["ms_per_step"] for r in per)  # TFLOP/s x ms
+    peaks, peak_src = read_peaks()
+    bf = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    return {"workload": "packed_8k", "seeds": n, "ms_per_step_mean": t / n,
+            "tflops_nontrivial_rows": fl / t, "frac_of_bf16_peak": fl / t / bf,
+            "nontrivial_rows_mean": sum(r["nontrivial_rows"] for r in per) / n,
+            "per_seed_ms": [round(r["ms_per_step"], 5) for r in per],
+            "per_seed_nontrivial_rows": [r["nontrivial_rows"] for r in per],
+            "peak_source": f"{peak_src} bf16_tflops"}
 
 
 def decode_bytes(wl):
@@ -732,6 +757,9 @@ def main():
                          "fused path (comparison only)")
     ap.add_argument("--no-side", action="store_true",
                     help="skip the decode and packed-document legs reported beside the headline")
+    ap.add_argument("--packed-seeds", type=int, default=0,
+                    help="also time the packed-document workload over seeds 0..N-1 and report the average "
+                         "(about 3 s of input generation per seed)")
     ap.add_argument("--gather", action="store_true",
                     help="also time the gather of the selected compressed rows (reported, not in the step)")
     args = ap.parse_args()
