@@ -579,9 +579,12 @@ __device__ void write_visible_set(int32_t* out, int K, int nvis, int tfirst, int
 //    behind.
 //  * In a round that also holds scored items, the trivial items whose rows
 //    each keep one contiguous run of visible entries -- the usual case with
-//    documents -- are written by warp 1 itself (after it has posted the
-//    round's select entries), so the select warps spend their time on the
-//    selections.
+//    documents -- are written by the scheduler warps themselves, so the
+//    select warps spend their time on the selections: the even-ranked ones
+//    of the round by warp 1 (after it has posted the round's select
+//    entries), the odd-ranked ones by warp 0 in a second pass over its
+//    rounds once it has posted every item (its posts keep the tensor cores
+//    fed; a single warp writing them all finished last on packed inputs).
 //  * Every other item is an entry of the select warps' ring; entry e is
 //    posted by warp e % 2 (the slot's parity is the entry's, so every slot
 //    has one writer, written in order), and the ring ends with a marker.
@@ -640,7 +643,7 @@ __device__ void run_scheduler_docs(const KParams& p, const Smem<C>& sm, const Wa
       }
     }
     const bool mixed = __ballot_sync(0xFFFFFFFFu, scored_l) != 0u;
-    const bool w1_l = mixed && ctriv_l;  // written by warp 1
+    const bool w1_l = mixed && ctriv_l;  // written by the scheduler warps
     const uint32_t sel_mask = __ballot_sync(0xFFFFFFFFu, my_it < n_mine && !w1_l);
     const int cnt = min(32, n_mine - it0);
     for (int k = 0; k < cnt; ++k) {
@@ -708,10 +711,11 @@ __device__ void run_scheduler_docs(const KParams& p, const Smem<C>& sm, const Wa
       ++posted;
     }
     if (sw == 1 && mixed) {
-      // the round's contiguous trivial items: each row's visible entries
-      // tfirst .. tfirst + nvis - 1, -1 padded
+      // the round's even-ranked contiguous trivial items: each row's visible
+      // entries tfirst .. tfirst + nvis - 1, -1 padded
+      const uint32_t w1_mask = __ballot_sync(0xFFFFFFFFu, w1_l);
       for (int k = 0; k < cnt; ++k) {
-        if (!__shfl_sync(0xFFFFFFFFu, w1_l, k)) continue;
+        if (!((w1_mask >> k) & 1u) || (__popc(w1_mask & ((1u << k) - 1u)) & 1)) continue;
         const int b = __shfl_sync(0xFFFFFFFFu, b_l, k);
         const int rb = __shfl_sync(0xFFFFFFFFu, rb_l, k);
 #pragma unroll
@@ -741,6 +745,42 @@ __device__ void run_scheduler_docs(const KParams& p, const Smem<C>& sm, const Wa
     if (lane == 0) sm.desc(slot)->b = -1;
     __syncwarp();
     if (lane == 0) mbar_arrive(sm.item_full(slot));
+    // second pass: the odd-ranked contiguous trivial items of the rounds
+    // that also hold scored items (the same classification as above)
+    for (int it0 = 0; it0 < n_mine; it0 += 32) {
+      const int my_it = it0 + (int)lane;
+      int b_l = 0, rb_l = 0, c_l = 0;
+      SegInfo si_l{};
+      bool scored_l = false, ctriv_l = false;
+      if (my_it < n_mine) {
+        sched_coords<C>(p, my_it, n_mine, b_l, rb_l, c_l);
+        si_l = p.seginfo[(size_t)b_l * p.n_rb + rb_l];
+        bool triv = can_trivial, contig = true;
+#pragma unroll
+        for (int j = 0; j < R; ++j) {
+          triv = triv && si_l.nvis[j] <= p.K;
+          contig = contig && si_l.contig[j] != 0;
+        }
+        scored_l = !triv;
+        ctriv_l = triv && contig;
+      }
+      if (__ballot_sync(0xFFFFFFFFu, scored_l) == 0u) continue;
+      const uint32_t w1_mask = __ballot_sync(0xFFFFFFFFu, ctriv_l);
+      const int cnt = min(32, n_mine - it0);
+      for (int k = 0; k < cnt; ++k) {
+        if (!((w1_mask >> k) & 1u) || !(__popc(w1_mask & ((1u << k) - 1u)) & 1)) continue;
+        const int b = __shfl_sync(0xFFFFFFFFu, b_l, k);
+        const int rb = __shfl_sync(0xFFFFFFFFu, rb_l, k);
+#pragma unroll
+        for (int j = 0; j < R; ++j) {
+          const int nv = __shfl_sync(0xFFFFFFFFu, si_l.nvis[j], k);
+          const int tf = __shfl_sync(0xFFFFFFFFu, si_l.tfirst[j], k);
+          const int s = rb * R + j;
+          if (s < p.S)
+            write_visible_set<32>(p.idx + ((size_t)b * p.S + s) * p.K, p.K, nv, tf, 1, 0, 0, nullptr, nullptr, team);
+        }
+      }
+    }
   }
 }
 
