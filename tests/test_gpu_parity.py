@@ -249,6 +249,22 @@ def _edge_inputs(c, seed=0, segs=None, w_dtype="bf16"):
         g = torch.Generator().manual_seed(seed + 9)
         inp.q_seg = torch.randint(0, 3, (wl.B, wl.S), generator=g, dtype=torch.int32)
         inp.kv_seg = torch.randint(0, 3, (wl.B, wl.W), generator=g, dtype=torch.int32)
+    elif segs == "many":  # nine scattered ids: most blocks of 128 rows hold more than four
+        g = torch.Generator().manual_seed(seed + 11)
+        inp.q_seg = torch.randint(0, 9, (wl.B, wl.S), generator=g, dtype=torch.int32)
+        inp.kv_seg = torch.randint(0, 9, (wl.B, wl.W), generator=g, dtype=torch.int32)
+    elif segs == "short_docs":  # contiguous documents of 4..40 rows: many per block of 128 rows
+        g = torch.Generator().manual_seed(seed + 13)
+        q_seg = torch.zeros(wl.B, wl.S, dtype=torch.int32)
+        for b in range(wl.B):
+            s, d = 0, 0
+            while s < wl.S:
+                n = int(torch.randint(4, 41, (1,), generator=g))
+                q_seg[b, s:s + n] = d
+                s, d = s + n, d + 1
+        last = (torch.arange(wl.W) * wl.compress_rate + wl.compress_rate - 1).clamp(max=wl.S - 1)
+        inp.q_seg = q_seg
+        inp.kv_seg = q_seg[:, last].contiguous()
     return inp
 
 
@@ -276,10 +292,18 @@ def test_edge_shapes(ci):
     _check_all(_edge_inputs(EDGE[ci], seed=ci))
 
 
-@pytest.mark.parametrize("segs", ["packed", "scattered"])
+@pytest.mark.parametrize("segs", ["packed", "scattered", "many", "short_docs"])
 @pytest.mark.parametrize("ci", [0, 3, 4])
 def test_edge_segments(ci, segs):
     _check_all(_edge_inputs(EDGE[ci], seed=10 + ci, segs=segs))
+
+
+@pytest.mark.parametrize("segs", ["many", "short_docs"])
+def test_segment_summaries_past_four_ids(segs):
+    """Blocks of 128 rows with more than four row ids (scattered, or many
+    short documents) on the 64-head fused path: rows beyond the first four
+    ids are summarised one by one."""
+    _check_all(_edge_inputs(dict(B=2, S=700, W=175, H=64, D=128, r=4, top_k=12), seed=31, segs=segs))
 
 
 def test_fp32_weights_large_heads():
